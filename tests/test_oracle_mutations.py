@@ -1,0 +1,82 @@
+"""Evidence that the oracle pins are strong: plant one plausible mistake at a
+time in a copy of the oracle's C source (on the CPU), build it, swap it in, and
+check that at least one pin in ``test_oracle_pins.py`` fails.
+"""
+import ctypes
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "cider_oracle.c")
+HDR = os.path.join(os.path.dirname(oracle.__file__), "cider_oracle.h")
+
+# (name, original text, planted mistake)
+MUTATIONS = [
+    ("round_half_away", "float r = nearbyintf(v / scale);", "float r = roundf(v / scale);"),
+    ("reciprocal_multiply", "float r = nearbyintf(v / scale);",
+     "float r = nearbyintf(v * (1.0f / scale));"),
+    ("zero_block_scale", "return (amax == 0.0f) ? 1.0f : amax / qdiv;", "return amax / qdiv;"),
+    ("scale_by_128", "float s = block_scale(amax, 127.0f);", "float s = block_scale(amax, 128.0f);"),
+    ("int4_qdiv_8", "quantize_weight(W, N, K, group_size, 7.0f, -8, 7, q4, sw);",
+     "quantize_weight(W, N, K, group_size, 8.0f, -8, 7, q4, sw);"),
+    ("nibble_order", "unsigned lo = (unsigned)(q[n * K + 2 * j] & 0xF);",
+     "unsigned lo = (unsigned)(q[n * K + 2 * j + 1] & 0xF);"),
+    ("nibble_sign", "return (t < 8u) ? (int)t : (int)t - 16;", "return (t < 8u) ? (int)t : (int)t - 8;"),
+    ("gemm_transposed", "s += (int64_t)qa[m * K + k] * (int64_t)qw[n * K + k];",
+     "s += (int64_t)qa[m * K + k] * (int64_t)qw[(k % N) * K + n % K];"),
+    ("gemm_dropped_term", "for (int64_t j = 0; j < gs; ++j) {\n          int64_t k",
+     "for (int64_t j = 1; j < gs; ++j) {\n          int64_t k"),
+    ("pg_reversed_order", "for (int64_t g = 0; g < G; ++g) {\n        float scale",
+     "for (int64_t g = G - 1; g >= 0; --g) {\n        float scale"),
+    ("pc_dropped_weight_scale", "v = v * sw[n];", "v = v * 1.0f;"),
+    ("act_amax_signed", "float a = fabsf(f16_bits_to_f32(row[k]));", "float a = f16_bits_to_f32(row[k]);"),
+]
+
+PIN_TESTS = [
+    pins.test_quantize_act_hand_worked_cases,
+    lambda: pins.test_quantize_act_brute_force_all_fp16_below_amax(3.140625),
+    lambda: pins.test_quantize_act_brute_force_all_fp16_below_amax(1000.0),
+    lambda: pins.test_quantize_act_brute_force_all_fp16_below_amax(0.0016956329345703125),
+    pins.test_quantize_act_zero_row_and_signs,
+    pins.test_weight_quant_hand_worked_cases,
+    lambda: pins.test_weight_quant_matches_independent_blockwise(64, 8),
+    lambda: pins.test_weight_quant_matches_independent_blockwise(0, 4),
+    pins.test_int4_nibbles_hand_worked,
+    pins.test_int4_unpack_exhaustive_and_pack_roundtrip,
+    pins.test_gemm_closed_forms,
+    pins.test_gemm_brute_force_python_ints_and_group_sums,
+    pins.test_gemm_is_not_transposed,
+    pins.test_dequant_pc_special_cases,
+    pins.test_dequant_pc_exact_emulation,
+    pins.test_dequant_pg_order_hand_worked,
+    pins.test_dequant_pg_exact_emulation,
+]
+
+
+@pytest.mark.parametrize("name,orig,bad", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(tmp_path, name, orig, bad):
+    src = open(SRC).read()
+    assert src.count(orig) >= 1, f"mutation anchor for {name} not found"
+    shutil.copy(HDR, tmp_path / "cider_oracle.h")
+    (tmp_path / "cider_oracle.c").write_text(src.replace(orig, bad))
+    so = tmp_path / "libmut.so"
+    subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-std=c11", "-fPIC", "-shared",
+                           "-o", str(so), str(tmp_path / "cider_oracle.c"), "-lm"])
+    mutated = oracle._configure(ctypes.CDLL(str(so)))
+    saved = oracle._load()
+    caught = []
+    try:
+        oracle._lib = mutated
+        for t in PIN_TESTS:
+            try:
+                t()
+            except (AssertionError, OverflowError, ValueError):
+                caught.append(getattr(t, "__name__", "lambda"))
+    finally:
+        oracle._lib = saved
+    assert caught, f"no pin caught the planted mistake {name}"

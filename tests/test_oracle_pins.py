@@ -1,0 +1,347 @@
+"""Pins for the CPU oracle: checks against facts fixed by the Cider README
+(page "cider") and by mathematics, never against the oracle itself.
+
+Each pin is chosen so that a plausible mistake in the oracle (a dropped term,
+a wrong sign or index, round-half-away instead of half-even, a reciprocal
+multiply instead of a divide, a transposed operand, a reversed group order)
+fails at least one of them; ``test_oracle_mutations.py`` plants such mistakes
+in a copy of the oracle and checks that these pins catch them.
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _blocks(path, keys):
+    cur, out = {}, []
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split(":", 1)
+            cur[k.strip()] = v.split()
+            if all(kk in cur for kk in keys):
+                out.append(cur)
+                cur = {}
+    return out
+
+
+# ------------------------------------------------------------ fp16 plumbing
+def test_f16_decode_all_bit_patterns_match_numpy():
+    """fp16 -> fp32 is exact; compare every bit pattern with numpy's decoder."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float32)
+    got = np.array([oracle.f16_to_f32(int(b)) for b in bits[::257]], np.float32)
+    np.testing.assert_array_equal(got, ref[::257])
+
+
+def test_f32_to_f16_rounds_to_nearest_even_like_numpy():
+    rng = np.random.default_rng(5)
+    vals = np.concatenate([rng.standard_normal(3000).astype(np.float32) * 1000,
+                           np.float32([65504, 65519.99, 65520, 1e-8, 2 ** -25, 3 * 2 ** -26,
+                                       1 + 2 ** -11, 1 + 3 * 2 ** -11, -0.0])])
+    got = np.array([oracle.f32_to_f16(float(v)) for v in vals], np.uint16)
+    with np.errstate(over="ignore"):
+        ref = vals.astype(np.float16).view(np.uint16)
+    np.testing.assert_array_equal(got, ref)
+
+
+# ------------------------------------------------------------ a1 activation quant
+def test_quantize_act_hand_worked_cases():
+    for case in _blocks(os.path.join(GOLDEN, "quant_act_hand.txt"), ("x", "q", "s")):
+        x = np.array([float(v) for v in case["x"]], np.float16)[None, :]
+        qa, sa = oracle.quantize_act(x)
+        assert qa[0].tolist() == [int(v) for v in case["q"]], case
+        assert sa[0] == np.float32(float(case["s"][0]))
+
+
+def _f32_div(a, b):
+    """Correctly rounded binary32 a/b, from the exact quotient in binary64
+    (53 >= 2*24 + 2, so rounding the double quotient to float is exact RN)."""
+    return (np.asarray(a, np.float64) / np.asarray(b, np.float64)).astype(np.float32)
+
+
+def _independent_quant_row(x16, qmax=127):
+    xf = x16.astype(np.float64)
+    amax = np.max(np.abs(xf))
+    s = np.float32(1.0) if amax == 0 else _f32_div(amax, qmax)
+    q = np.rint(_f32_div(xf, s).astype(np.float64))
+    return np.clip(q, -qmax, qmax).astype(np.int8), np.float32(s)
+
+
+# 0.0016956329345703125 and 0.50732421875 are amax values for which an IEEE
+# divide and a reciprocal multiply give different codes for some fp16 x.
+@pytest.mark.parametrize("amax", [65504.0, 1.0, 127.0, 3.140625, 0.0009765625,
+                                  2.0 ** -24 * 37, 2.0 ** -14, 1000.0,
+                                  0.0016956329345703125, 0.50732421875])
+def test_quantize_act_brute_force_all_fp16_below_amax(amax):
+    """Every fp16 value with |x| <= amax, quantized in rows that contain amax,
+    against an independent binary64 computation of the same fp32 steps."""
+    allv = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16).view(np.float16)
+    ok = np.isfinite(allv) & (np.abs(allv.astype(np.float64)) <= amax)
+    vals = allv[ok]
+    W = 1024
+    pad = (-len(vals)) % (W - 1)
+    vals = np.concatenate([vals, np.zeros(pad, np.float16)]).reshape(-1, W - 1)
+    x = np.concatenate([np.full((vals.shape[0], 1), amax, np.float16), vals], axis=1)
+    qa, sa = oracle.quantize_act(x)
+    for r in range(x.shape[0]):
+        qref, sref = _independent_quant_row(x[r])
+        assert sa[r] == sref
+        np.testing.assert_array_equal(qa[r], qref)
+    assert np.all(qa[:, 0] == 127)
+
+
+def test_quantize_act_zero_row_and_signs():
+    x = np.zeros((3, 64), np.float16)
+    x[1, 5] = -3.0
+    x[2] = np.linspace(-2, 2, 64).astype(np.float16)
+    qa, sa = oracle.quantize_act(x)
+    assert sa[0] == 1.0 and not qa[0].any()
+    assert qa[1, 5] == -127 and np.count_nonzero(qa[1]) == 1
+    assert qa[2, 0] == -127 and qa[2, -1] == 127
+    # symmetric: negating x negates q and keeps s
+    qn, sn = oracle.quantize_act(-x)
+    np.testing.assert_array_equal(qn, -qa)
+    np.testing.assert_array_equal(sn, sa)
+
+
+def test_quantize_act_random_rows_match_independent():
+    from w4a8_quantized_linear_gb300 import inputs
+    x = inputs.activations(37, 320, seed=11)
+    qa, sa = oracle.quantize_act(x)
+    for r in range(x.shape[0]):
+        qref, sref = _independent_quant_row(x[r])
+        assert sa[r] == sref
+        np.testing.assert_array_equal(qa[r], qref)
+
+
+# ------------------------------------------------------------ a2 weight quant
+def test_weight_quant_hand_worked_cases():
+    path = os.path.join(GOLDEN, "weight_quant_hand.txt")
+    rows = []
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            bits, rest = line.split(None, 1)
+            key, vals = rest.split(":", 1)
+            rows.append((int(bits), key.strip(), vals.split()))
+    for i in range(0, len(rows), 3):
+        bits = rows[i][0]
+        w = np.array([float(v) for v in rows[i][2]], np.float32)[None, :]
+        fn = oracle.quantize_weight_int8 if bits == 8 else oracle.quantize_weight_int4
+        q, s = fn(w, 0)
+        assert q[0].tolist() == [int(v) for v in rows[i + 1][2]]
+        assert s[0, 0] == np.float32(float(rows[i + 2][2][0]))
+
+
+@pytest.mark.parametrize("gs", [0, 64, 128])
+@pytest.mark.parametrize("bits", [8, 4])
+def test_weight_quant_matches_independent_blockwise(gs, bits):
+    from w4a8_quantized_linear_gb300 import inputs
+    W = inputs.weights(9, 256, seed=3)
+    W[2, :] = 0.0                      # zero row
+    W[3, 64:128] = 0.0                 # zero block
+    W[4, 7] = 0.5                      # dominant element
+    qmax, qmin = (127, -127) if bits == 8 else (7, -8)
+    fn = oracle.quantize_weight_int8 if bits == 8 else oracle.quantize_weight_int4
+    q, s = fn(W, gs)
+    g = gs or 256
+    G = 256 // g
+    assert s.shape == (9, G)
+    for n in range(9):
+        for j in range(G):
+            blk = W[n, j * g:(j + 1) * g].astype(np.float64)
+            amax = np.max(np.abs(blk))
+            sref = np.float32(1.0) if amax == 0 else _f32_div(amax, qmax)
+            qref = np.clip(np.rint(_f32_div(blk, sref).astype(np.float64)), qmin, qmax)
+            assert s[n, j] == sref
+            np.testing.assert_array_equal(q[n, j * g:(j + 1) * g], qref.astype(np.int8))
+    assert np.abs(q).max() <= qmax and q.min() >= qmin
+    # the element holding the block maximum maps to +-qmax
+    assert q[4, 7] == qmax
+
+
+# ------------------------------------------------------------ a4 int4 packing
+def test_int4_nibbles_hand_worked():
+    with open(os.path.join(GOLDEN, "int4_nibbles.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    packed = np.array([[int(r[0], 16) for r in rows]], np.uint8)
+    q = oracle.unpack_int4(packed)[0]
+    for i, r in enumerate(rows):
+        assert (q[2 * i], q[2 * i + 1]) == (int(r[1]), int(r[2])), r
+
+
+def test_int4_unpack_exhaustive_and_pack_roundtrip():
+    allb = np.arange(256, dtype=np.uint8)[None, :]
+    q = oracle.unpack_int4(allb)[0]
+    for b in range(256):
+        lo, hi = b & 15, b >> 4
+        assert q[2 * b] == (lo - 16 if lo >= 8 else lo)
+        assert q[2 * b + 1] == (hi - 16 if hi >= 8 else hi)
+    np.testing.assert_array_equal(oracle.pack_int4(q[None, :]), allb)
+    vals = np.array([(a, b) for a in range(-8, 8) for b in range(-8, 8)], np.int8).reshape(1, -1)
+    np.testing.assert_array_equal(oracle.unpack_int4(oracle.pack_int4(vals)), vals)
+
+
+# ------------------------------------------------------------ a3 integer GEMM
+def test_gemm_closed_forms():
+    K = 640
+    a = np.full((2, K), 127, np.int8)
+    w = np.full((3, K), 127, np.int8)
+    assert np.all(oracle.gemm_acc(a, w) == 16129 * K)
+    alt = np.tile(np.array([127, -127], np.int8), K // 2)[None, :]
+    assert np.all(oracle.gemm_acc(alt, w) == 0)
+    assert np.all(oracle.gemm_acc(a, -w) == -16129 * K)
+    # selector weights pick activation columns: acc[m,n] = qa[m, sel[n]] * 1
+    rng = np.random.default_rng(2)
+    qa = rng.integers(-127, 128, (5, K), dtype=np.int8)
+    sel = np.array([0, 3, K - 1, 200])
+    qw = np.zeros((4, K), np.int8)
+    qw[np.arange(4), sel] = 1
+    np.testing.assert_array_equal(oracle.gemm_acc(qa, qw)[:, :, 0], qa[:, sel])
+    # a weight row that is a basis vector times -7 at column 5
+    qw2 = np.zeros((1, K), np.int8)
+    qw2[0, 5] = -7
+    np.testing.assert_array_equal(oracle.gemm_acc(qa, qw2)[:, 0, 0], -7 * qa[:, 5].astype(np.int32))
+
+
+def test_gemm_brute_force_python_ints_and_group_sums():
+    rng = np.random.default_rng(4)
+    M, N, K = 3, 4, 256
+    qa = rng.integers(-127, 128, (M, K), dtype=np.int8)
+    qw = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    for gs in (0, 64, 128):
+        acc = oracle.gemm_acc(qa, qw, gs)
+        g = gs or K
+        for m in range(M):
+            for n in range(N):
+                for j in range(K // g):
+                    ref = sum(int(qa[m, k]) * int(qw[n, k]) for k in range(j * g, (j + 1) * g))
+                    assert acc[m, n, j] == ref
+        # invariant: group accumulators sum to the per-channel one
+        np.testing.assert_array_equal(acc.sum(axis=2), oracle.gemm_acc(qa, qw, 0)[:, :, 0])
+
+
+def test_gemm_is_not_transposed():
+    """Non-square case where acc[m,n] = <qa[m], qw[n]> differs from any
+    transposed reading."""
+    qa = np.array([[1, 2, 0, 0], [0, 0, 3, 0]], np.int8)
+    qw = np.array([[1, 0, 0, 0], [0, 1, 0, 0], [0, 0, 0, 1]], np.int8)
+    acc = oracle.gemm_acc(qa, qw)[:, :, 0]
+    np.testing.assert_array_equal(acc, [[1, 2, 0], [0, 0, 0]])
+
+
+def test_gemm_overflow_is_reported():
+    K = 133184                       # 16129 * K > 2^31 - 1
+    a = np.full((1, K), 127, np.int8)
+    with pytest.raises(OverflowError):
+        oracle.gemm_acc(a, a)
+
+
+# ------------------------------------------------------------ a5 dequant
+def _r32(v):
+    """Round an exact rational / double to binary32 (RN)."""
+    return np.float32(float(v))
+
+
+def test_dequant_pc_special_cases():
+    acc = np.arange(-2048, 2049, dtype=np.int32)[None, :]
+    N = acc.shape[1]
+    y = oracle.dequant_pc(acc, np.float32([1.0]), np.ones(N, np.float32))
+    np.testing.assert_array_equal(y.astype(np.float64), acc.astype(np.float64))
+    # scaling s_w by 2 doubles y exactly (no overflow at these magnitudes)
+    rng = np.random.default_rng(7)
+    acc = rng.integers(-10 ** 6, 10 ** 6, (4, 50)).astype(np.int32)
+    sa = rng.uniform(1e-3, 1e-1, 4).astype(np.float32)
+    sw = rng.uniform(1e-5, 1e-3, 50).astype(np.float32)
+    y1 = oracle.dequant_pc(acc, sa, sw)
+    y2 = oracle.dequant_pc(acc, sa, sw * 2)
+    np.testing.assert_array_equal(y2.astype(np.float32), y1.astype(np.float32) * 2)
+    # overflow saturates to inf
+    yo = oracle.dequant_pc(np.int32([[10 ** 9]]), np.float32([1.0]), np.float32([1.0]))
+    assert np.isinf(yo[0, 0])
+
+
+def test_dequant_pc_exact_emulation():
+    """((float(acc) * s_a) * s_w) in binary32, emulated with exact rationals and
+    one rounding per operation, then rounded to fp16."""
+    rng = np.random.default_rng(8)
+    acc = rng.integers(-(2 ** 27), 2 ** 27, (6, 40)).astype(np.int32)
+    sa = rng.uniform(1e-4, 1.0, 6).astype(np.float32)
+    sw = rng.uniform(1e-6, 1e-4, 40).astype(np.float32)
+    y = oracle.dequant_pc(acc, sa, sw)
+    for m in range(6):
+        for n in range(40):
+            a = _r32(int(acc[m, n]))                   # int32 -> fp32 RN
+            t = _r32(Fraction(float(a)) * Fraction(float(sa[m])))
+            t = _r32(Fraction(float(t)) * Fraction(float(sw[n])))
+            assert y[m, n] == np.float16(t)
+
+
+def test_dequant_pg_order_hand_worked():
+    with open(os.path.join(GOLDEN, "dequant_order.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    for r in rows:
+        acc = np.array([[[int(r[0]), int(r[1]), int(r[2])]]], np.int32)
+        y = oracle.dequant_pg(acc, np.float32([1.0]), np.ones((1, 3), np.float32))
+        assert float(y[0, 0]) == float(r[3]), r
+
+
+def test_dequant_pg_exact_emulation():
+    rng = np.random.default_rng(9)
+    M, N, G = 5, 7, 20
+    acc = rng.integers(-(2 ** 21), 2 ** 21, (M, N, G)).astype(np.int32)
+    sa = rng.uniform(1e-3, 1.0, M).astype(np.float32)
+    sw = rng.uniform(1e-5, 1e-2, (N, G)).astype(np.float32)
+    y = oracle.dequant_pg(acc, sa, sw)
+    for m in range(M):
+        for n in range(N):
+            s = np.float32(0)
+            for g in range(G):
+                sc = _r32(Fraction(float(sa[m])) * Fraction(float(sw[n, g])))
+                term = _r32(Fraction(float(sc)) * int(acc[m, n, g]))
+                s = _r32(Fraction(float(s)) + Fraction(float(term)))
+            assert y[m, n] == np.float16(s)
+
+
+# ------------------------------------------------------------ whole layer
+def test_linear_is_composition_and_rows_are_independent():
+    from w4a8_quantized_linear_gb300 import inputs
+    x, W = inputs.layer(19, 48, 256)
+    for gs in (0, 64, 128):
+        qw, sw = oracle.quantize_weight_int8(W, gs)
+        qa, sa = oracle.quantize_act(x)
+        acc = oracle.gemm_acc(qa, qw, gs)
+        yref = oracle.dequant_pg(acc, sa, sw) if gs else oracle.dequant_pc(acc, sa, sw)
+        y = oracle.linear(x, qw, sw, gs)
+        np.testing.assert_array_equal(y.view(np.uint16), yref.view(np.uint16))
+        rows = [18, 3, 7]
+        np.testing.assert_array_equal(oracle.linear(x, qw, sw, gs, rows=rows).view(np.uint16),
+                                      yref[rows].view(np.uint16))
+        np.testing.assert_array_equal(oracle.linear(x, qw, sw, gs, threads=4).view(np.uint16),
+                                      yref.view(np.uint16))
+
+
+def test_linear_close_to_unquantized_product():
+    """Sanity (not a parity pin): the quantized layer approximates x W^T."""
+    from w4a8_quantized_linear_gb300 import inputs
+    x, W = inputs.layer(32, 64, 512)
+    ref = x.astype(np.float64) @ W.astype(np.float64).T
+    for bits, gs in ((8, 0), (8, 128), (4, 128)):
+        if bits == 8:
+            qw, sw = oracle.quantize_weight_int8(W, gs)
+        else:
+            qw, sw = oracle.quantize_weight_int4(W, gs)
+        y = oracle.linear(x, qw, sw, gs).astype(np.float64)
+        cos = (y * ref).sum() / np.sqrt((y * y).sum() * (ref * ref).sum())
+        assert cos > (0.99 if bits == 8 else 0.95), (bits, gs, cos)
