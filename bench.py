@@ -1,0 +1,435 @@
+#!/usr/bin/env python
+"""Benchmark of the W8A8 / W4A8 online-activation-quantized linear on GB300.
+
+One step = one whole layer call through the public API (per-token activation
+quantization + integer GEMM with fused dequant) on one batch of seeded
+synthetic inputs already resident in HBM.  The default workload is the W8A8
+per-channel linear at M=4096, N=10240, K=2560, on which the metric is quoted.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints ONE JSON line on stdout (rank 0).  Under torchrun every rank runs the
+same workload on its own GPU (replicas: the layer has no exchange step), and
+the value is the sum of all ranks' work over the slowest rank's time.
+
+Timing: CUDA events on the launching stream around exactly K steps, bracketed
+by a barrier and a device synchronize; inputs, weights and outputs rotate
+through enough sets to exceed twice the L2 size, so every step reads HBM.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "W8A8 linear TOPS @M=4096 N=10240 K=2560; % of INT8/HBM roofline"
+UNIT = "TOPS"
+# The pages' own number for this workload: 4.41 ms on an Apple M5 Pro
+# (per-channel W8A8, N=10240, K=2560, M=4096) = 48.7 TOPS.  Context only.
+PAGES_TOPS = 2 * 4096 * 10240 * 2560 / 4.41e-3 / 1e12
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--M", type=int, default=4096)
+    ap.add_argument("--N", type=int, default=10240)
+    ap.add_argument("--K", type=int, default=2560)
+    ap.add_argument("--gs", type=int, default=0, help="0 = per channel, else 64 / 128")
+    ap.add_argument("--bits", type=int, default=8, choices=[8, 4])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    a.warmup = max(a.warmup, 3)
+    return a
+
+
+def workload_name(a):
+    gran = f"per-group gs={a.gs}" if a.gs else "per-channel"
+    return f"W{a.bits}A8 {gran} linear M={a.M} N={a.N} K={a.K}"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={CLOCK_QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            f = [s.strip() for s in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((ts, float(f[1]), float(f[2]), f))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if self.t0 <= r[0] <= self.t1 + 0.2]
+        use = inside or sorted(rows, key=lambda r: abs(r[0] - self.t0))[:2]
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for r in use:
+            for nm, v in zip(names[1:], r[3][5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use),
+                "reasons": sorted(reasons), "samples": len(use),
+                "in_timed_region": bool(inside)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "w4a8_quantized_linear_gb300", "csrc")
+    for name in ("gemm_tc.cu", "gemv.cu", "cider_device.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source and workload."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_source_sha") != kernel_source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def make_host_inputs(a, rank: int, n_sets: int):
+    from w4a8_quantized_linear_gb300 import inputs
+    xs, ws = [], []
+    for s in range(n_sets):
+        x, w = inputs.layer(a.M, a.N, a.K, base_seed=1000 * rank, index=s)
+        xs.append(x)
+        ws.append(w)
+    return xs, ws
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(a):
+    """The oracle (plain single-threaded C) on the host cores, on a bounded
+    sample of rows per step of the same workload."""
+    import oracle
+    from w4a8_quantized_linear_gb300 import inputs
+
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    oracle.build()
+    x, W = inputs.layer(a.M, a.N, a.K)
+    if a.bits == 8:
+        qv, sw = oracle.quantize_weight_int8(W, a.gs)
+    else:
+        qv, sw = oracle.quantize_weight_int4(W, a.gs)
+    # calibrate: one row
+    t = time.perf_counter()
+    oracle.linear(x, qv, sw, a.gs, rows=[0])
+    row_s = time.perf_counter() - t
+    budget = 120.0
+    rows_per_step = int(max(1, min(16, budget / max(row_s, 1e-6) / (a.steps + a.warmup))))
+    rng = np.random.default_rng(0)
+    for _ in range(a.warmup):
+        oracle.linear(x, qv, sw, a.gs, rows=rng.integers(0, a.M, rows_per_step))
+    t = time.perf_counter()
+    for _ in range(a.steps):
+        oracle.linear(x, qv, sw, a.gs, rows=rng.integers(0, a.M, rows_per_step))
+    el = time.perf_counter() - t
+    ops = 2.0 * rows_per_step * a.N * a.K * a.steps
+    val = ops / el / 1e12
+    sample = (f"{rows_per_step} random rows of {a.M} per step (all N={a.N}, K={a.K}), "
+              f"single-threaded C oracle, {el:.1f} s timed")
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT,
+            "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": el / a.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": {"workload": workload_name(a), "M": a.M, "N": a.N, "K": a.K,
+                       "group_size": a.gs, "bits": a.bits,
+                       "note": "CPU oracle; each step computes a row sample of the workload"},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(a, x, qv, sw, budget_s=12.0):
+    """The oracle as it stands, timed on this host on a bounded row sample."""
+    import oracle
+    oracle.build()
+    rows, el = 0, 0.0
+    chunk = 4
+    t = time.perf_counter()
+    while el < budget_s and rows < a.M:
+        oracle.linear(x, qv, sw, a.gs, rows=np.arange(rows, min(rows + chunk, a.M)))
+        rows = min(rows + chunk, a.M)
+        el = time.perf_counter() - t
+    val = 2.0 * rows * a.N * a.K / el / 1e12
+    return {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of the {workload_name(a)} workload "
+                      f"({rows} x {a.N} x {a.K}), single-threaded C oracle, {el:.1f} s"}
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(a):
+    import torch
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from w4a8_quantized_linear_gb300 import _build
+    _build.build()
+    import w4a8_quantized_linear_gb300 as cider
+    if not cider.cider_is_available():
+        raise SystemExit("libcider: current device is not a supported sm_103 GPU")
+
+    set_bytes = 2 * a.M * a.K + (a.N * a.K if a.bits == 8 else a.N * a.K // 2) + 2 * a.M * a.N
+    n_sets = max(2, -(-2 * L2_BYTES // set_bytes) + 1)
+    log(f"[bench] {workload_name(a)}: {n_sets} rotating sets of {set_bytes / 1e6:.1f} MB")
+    xs_h, ws_h = make_host_inputs(a, rank, n_sets)
+    xs, qws, sws, ys = [], [], [], []
+    for x, w in zip(xs_h, ws_h):
+        xs.append(torch.from_numpy(x).to(dev))
+        wd = torch.from_numpy(w).to(dev)
+        if a.bits == 8:
+            q, s = cider.cider_quantize_weight_int8(wd, a.gs)
+        else:
+            q, s = cider.cider_quantize_weight_int4(wd, a.gs)
+        del wd
+        qws.append(q)
+        sws.append(s)
+        ys.append(torch.empty((a.M, a.N), dtype=torch.float16, device=dev))
+    lin = cider.cider_w8a8_linear if a.bits == 8 else cider.cider_w4a8_linear
+    torch.cuda.synchronize()
+
+    def step(i, ev=None):
+        s = i % n_sets
+        if ev is not None:
+            cider.cider_set_gemm_events(*ev)
+        lin(xs[s], qws[s], sws[s], a.gs, out=ys[s])
+
+    for i in range(a.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(a.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.5)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark(True)
+    start.record()
+    for i in range(a.steps):
+        step(i, evs[i])
+    stop.record()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark(False)
+    cider.cider_set_gemm_events(None, None)
+    if ws > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if clocks else None
+    el_ms = start.elapsed_time(stop)
+    gemm_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    if cider.cider_check_device_error() != 0:
+        raise SystemExit("libcider reported a timed-out wait inside a kernel")
+    if ws > 1:
+        t = torch.tensor([el_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        el_ms = float(t.item())
+
+    ops_step = 2.0 * a.M * a.N * a.K
+    value = ops_step * a.steps * ws / (el_ms * 1e-3) / 1e12
+    gemm_avg_s = statistics.fmean(gemm_ms) * 1e-3
+
+    # end to end through the public API with host buffers (copies inside the timed region)
+    e2e = None
+    n_e2e = max(3, min(a.e2e_steps, a.steps))
+    xh = [torch.from_numpy(x).pin_memory() for x in xs_h[:2]]
+    yh = [torch.empty((a.M, a.N), dtype=torch.float16).pin_memory() for _ in range(2)]
+    for i in range(3):
+        xs[i % 2].copy_(xh[i % 2], non_blocking=True)
+        lin(xs[i % 2], qws[i % 2], sws[i % 2], a.gs, out=ys[i % 2])
+        yh[i % 2].copy_(ys[i % 2], non_blocking=True)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(n_e2e):
+        s = i % 2
+        xs[s].copy_(xh[s], non_blocking=True)
+        lin(xs[s], qws[s], sws[s], a.gs, out=ys[s])
+        yh[s].copy_(ys[s], non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": ops_step * n_e2e * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+           "h2d_bytes_per_step": 2 * a.M * a.K, "d2h_bytes_per_step": 2 * a.M * a.N,
+           "steps": n_e2e}
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    peaks, peak_src = measured_peaks()
+    small_m = a.M <= 16
+    wl = workload_name(a)
+    if small_m:
+        wbytes = a.N * a.K if a.bits == 8 else a.N * a.K // 2
+        G = a.K // a.gs if a.gs else 1
+        alg_bytes = wbytes + 4 * a.N * G + a.M * a.K + 4 * a.M + 2 * a.M * a.N
+        achieved = alg_bytes / gemm_avg_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(wl),
+                "kernel": "gemv_kernel (small-M weight-streaming GEMV)",
+                "peak_source": f"{peak_src} hbm_gbs",
+                "algorithmic_bytes_per_launch": alg_bytes}
+    else:
+        long_region = el_ms > 1000.0
+        pk = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+        achieved = ops_step / gemm_avg_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
+                "frac": achieved / pk, "traffic": ncu_traffic(wl),
+                "kernel": "gemm_tc_kernel (tcgen05 kind::f16 on exact integer codes)",
+                "peak_source": (f"{peak_src} bf16_tflops"
+                                f"{'_sustained' if long_region else ''}"
+                                " x 1.0 (fp16 and bf16 dense tensor rates are equal)"),
+                "algorithmic_ops_per_launch": ops_step}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": el_ms / a.steps, "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": (value / PAGES_TOPS) if (a.M, a.N, a.K, a.gs, a.bits) == (4096, 10240, 2560, 0, 8) else None,
+        "dtype": "int8", "data": "synthetic",
+        "config": {"workload": wl, "M": a.M, "N": a.N, "K": a.K, "group_size": a.gs,
+                   "bits": a.bits, "parallelism": f"replicas x{ws}",
+                   "l2": f"inputs larger than L2: {n_sets} rotating x/qw/y sets "
+                         f"({n_sets * set_bytes / 1e6:.0f} MB)",
+                   "gemm_ms_avg": gemm_avg_s * 1e3},
+        "roofline": roof,
+        "gpu_launches": 2 * a.steps,
+        "e2e": e2e,
+        "clocks": clk,
+    }
+    if ws == 1 and not a.no_cpu_baseline:
+        import oracle
+        x0 = xs_h[0]
+        if a.bits == 8:
+            qv, sw = oracle.quantize_weight_int8(ws_h[0], a.gs)
+        else:
+            qv, sw = oracle.quantize_weight_int4(ws_h[0], a.gs)
+        line["cpu_baseline"] = cpu_baseline(a, x0, qv, sw)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    a = parse_args()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)
+
+
+if __name__ == "__main__":
+    main()

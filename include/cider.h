@@ -1,0 +1,188 @@
+/*
+ * cider.h -- C ABI of the GB300 (sm_103a) online-activation-quantized linear
+ * layer, W8A8 and W4A8.
+ *
+ * Operation (Cider README, page "cider"):
+ *   "Quantization" table -- activations symmetric INT8 per token; weights
+ *   symmetric INT8 per channel or per group (gs = 64 / 128), or INT4 packed two
+ *   per uint8 ("Modes" table, W4A8); INT32 accumulation; output dequant
+ *   C_fp16 = C_int32 * s_act * s_weight.
+ *   "Architecture / Metal kernel pipeline" -- quantize_per_token (fp16 ->
+ *   INT8 + per-token scale), then INT8 x INT8 -> INT32 -> FP16 with the scales
+ *   applied in the store.
+ *   "Low-level API" -- perchannel_linear(x, w_int8, scale) and
+ *   w4a8_linear(x, packed_w4, scale4) return fp16; quantize_weight_int8 and
+ *   pack_weight_int4 prepare weights.
+ * Precise definitions used here (the page leaves them open):
+ *   s_a[m] = max_k |x[m,k]| / 127 in fp32 (IEEE divide), 1 when the row is 0;
+ *   q_a[m,k] = clamp(rint(x[m,k] / s_a[m]), -127, 127), ties to even;
+ *   acc[m,n,g] = sum_{k in group g} q_a[m,k] * q_w[n,k]   (exact integer);
+ *   per channel: y[m,n] = fp16((float(acc) * s_a[m]) * s_w[n]);
+ *   per group:   y[m,n] = fp16(sum over g, increasing, of
+ *                               (s_a[m] * s_w[n,g]) * float(acc[m,n,g])).
+ *   INT4 weight values lie in [-8, 7]; byte j of a packed row holds element 2j
+ *   in its low nibble and element 2j+1 in its high nibble, two's complement.
+ *
+ * Conventions for every entry point
+ *   - Tensors are dense, row-major, caller-owned DEVICE memory on the current
+ *     CUDA device (for example PyTorch allocations).  The library keeps no
+ *     pointer after the call returns and holds no state besides a per-device
+ *     stream-ordered memory pool for its scratch buffers.
+ *   - fp16 tensors are IEEE binary16 (passed as void*).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is
+ *     enqueued on it; no entry point synchronizes.  Launch errors are returned
+ *     as CIDER_ERR_CUDA; faults inside kernels surface at the caller's next
+ *     synchronization, as with any CUDA library.
+ *   - Argument checks run on the host before any launch, in this order:
+ *     an empty problem (M == 0 or N == 0) returns CIDER_OK and launches
+ *     nothing; null pointers, negative sizes, K < 32, K % 32 != 0, N % 8 != 0,
+ *     a bad granularity / group size (per channel: group_size 0; per group:
+ *     group_size 64 or 128 with K % group_size == 0) give
+ *     CIDER_ERR_INVALID_ARGUMENT; a pointer not aligned to 16 bytes (fp16 and
+ *     integer matrices) or 4 bytes (fp32 scale vectors, int32 accumulators)
+ *     gives CIDER_ERR_MISALIGNED; a current device that is not sm_103 gives
+ *     CIDER_ERR_UNSUPPORTED_DEVICE.  There is no CPU fallback.
+ *   - Inputs must be finite; results for NaN / Inf inputs are unspecified.
+ */
+#ifndef CIDER_H
+#define CIDER_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CIDER_OK = 0,
+  CIDER_ERR_INVALID_ARGUMENT = 1,
+  CIDER_ERR_MISALIGNED = 2,
+  CIDER_ERR_UNSUPPORTED_DEVICE = 3,
+  CIDER_ERR_CUDA = 4,
+  CIDER_ERR_TIMEOUT = 5
+} cider_status_t;
+
+typedef enum { CIDER_PER_CHANNEL = 0, CIDER_PER_GROUP = 1 } cider_granularity_t;
+
+/* 1 when the current CUDA device is an sm_103 GPU this library was built
+ * for, else 0 (the Cider README's is_available(), "Conditional compilation").
+ * The environment variable CIDER_FORCE_UNSUPPORTED=1 forces 0. */
+int cider_is_available(void);
+
+/* Static, NUL-terminated description of a status code.  Never NULL. */
+const char* cider_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int cider_version(void);
+
+/* Per-token activation quantization (Cider README, "Metal kernel pipeline",
+ * step quantize_per_token).
+ *   x   fp16 [M, K]  input
+ *   qa  int8 [M, K]  output codes in [-127, 127]
+ *   sa  fp32 [M]     output per-token scales */
+cider_status_t cider_quantize_act(const void* x, int64_t M, int64_t K,
+                                  int8_t* qa, float* sa, void* stream);
+
+/* Symmetric min-max INT8 weight quantization (Cider README, "Notes": min-max
+ * scales; "Quantization": per channel or per group).  s_w = max|W| / 127 per
+ * row (group_size 0) or per group_size-element block (64 or 128),
+ * q = clamp(rint(W / s_w), -127, 127), an all-zero block gets s_w = 1.
+ *   w   fp32 [N, K]  input
+ *   qw  int8 [N, K]  output
+ *   sw  fp32 [N, G]  output, G = 1 (per channel) or K / group_size */
+cider_status_t cider_quantize_weight_int8(const float* w, int64_t N, int64_t K,
+                                          int group_size, int8_t* qw, float* sw,
+                                          void* stream);
+
+/* Symmetric min-max INT4 weight quantization and packing (Cider README,
+ * "Modes": W4A8 "INT4 packed (uint8)"; "Low-level API": pack_weight_int4).
+ * s_w = max|W| / 7 per row or group, q = clamp(rint(W / s_w), -8, 7), packed
+ * two per byte, element 2j in the low nibble.
+ *   w          fp32  [N, K]
+ *   qw_packed  uint8 [N, K/2]  output
+ *   sw         fp32  [N, G]    output */
+cider_status_t cider_quantize_weight_int4(const float* w, int64_t N, int64_t K,
+                                          int group_size, uint8_t* qw_packed,
+                                          float* sw, void* stream);
+
+/* W8A8 linear: y = dequant(quant(x) x qw^T) (Cider README, "Low-level API":
+ * perchannel_linear; "Metal kernel pipeline": quantize_per_token then
+ * matmul_fused_dequant).  Quantizes x per token on the device (scratch from
+ * the library's stream-ordered pool), then runs the integer GEMM with the
+ * dequant fused into its store.  M <= 16 uses the weight-streaming GEMV path,
+ * larger M the tensor-core GEMM.
+ *   x     fp16 [M, K]
+ *   qw    int8 [N, K]       (out_features x in_features, nn.Linear layout)
+ *   sw    fp32 [N] (granularity CIDER_PER_CHANNEL, group_size 0)
+ *         or   [N, K/group_size] (CIDER_PER_GROUP, group_size 64 or 128)
+ *   y     fp16 [M, N]       output */
+cider_status_t cider_w8a8_linear(const void* x, int64_t M, int64_t N, int64_t K,
+                                 const int8_t* qw, const float* sw,
+                                 int granularity, int group_size, void* y,
+                                 void* stream);
+
+/* W4A8 linear (Cider README, "Low-level API": w4a8_linear; "Architecture":
+ * INT4 -> INT8 unpack ahead of the matrix multiply).  As cider_w8a8_linear
+ * with qw_packed uint8 [N, K/2] holding INT4 values. */
+cider_status_t cider_w4a8_linear(const void* x, int64_t M, int64_t N, int64_t K,
+                                 const uint8_t* qw_packed, const float* sw,
+                                 int granularity, int group_size, void* y,
+                                 void* stream);
+
+/* The two linears with the activation already quantized (qa int8 [M, K],
+ * sa fp32 [M], as produced by cider_quantize_act).  Several projections that
+ * read the same input (Q/K/V, gate/up) quantize it once and share it
+ * (the idea of the pages' shared input preparation, "_InputGroup"). */
+cider_status_t cider_w8a8_linear_prequant(const int8_t* qa, const float* sa,
+                                          int64_t M, int64_t N, int64_t K,
+                                          const int8_t* qw, const float* sw,
+                                          int granularity, int group_size,
+                                          void* y, void* stream);
+cider_status_t cider_w4a8_linear_prequant(const int8_t* qa, const float* sa,
+                                          int64_t M, int64_t N, int64_t K,
+                                          const uint8_t* qw_packed,
+                                          const float* sw, int granularity,
+                                          int group_size, void* y, void* stream);
+
+/* Raw integer accumulators of the same kernels (the dispatch by M and the
+ * main loops of the linears above, with an int32 store in place of the
+ * dequant): acc[m, n, g] = sum over k in group g of qa[m,k] * q_w[n,k],
+ * layout [M, N, G], G = 1 for group_size 0 (one group spanning K), else
+ * K / group_size.  For verification.
+ *   qa  int8 [M, K];  qw int8 [N, K] or qw_packed uint8 [N, K/2];
+ *   acc int32 [M, N, G] output. */
+cider_status_t cider_w8a8_accumulators(const int8_t* qa, int64_t M, int64_t N,
+                                       int64_t K, const int8_t* qw,
+                                       int group_size, int32_t* acc,
+                                       void* stream);
+cider_status_t cider_w4a8_accumulators(const int8_t* qa, int64_t M, int64_t N,
+                                       int64_t K, const uint8_t* qw_packed,
+                                       int group_size, int32_t* acc,
+                                       void* stream);
+
+/* Optional timing hook for benchmarks.  When both events are non-NULL, every
+ * later linear / accumulator call made from the calling host thread records
+ * `ev_start` on its stream immediately before launching its integer-GEMM
+ * kernel (the tensor-core GEMM, or the GEMV for M <= 16) and `ev_stop`
+ * immediately after it, so cudaEventElapsedTime gives that kernel's device
+ * time.  Pass NULL, NULL to stop.  The events are caller-owned cudaEvent_t
+ * handles created with timing enabled.  Always returns CIDER_OK. */
+cider_status_t cider_set_gemm_events(void* ev_start, void* ev_stop);
+
+/* Device-side error word shared by the library's kernels on the current
+ * device.  Every wait inside a kernel is bounded; a wait that runs out sets
+ * this word and the kernel returns early instead of hanging.  This call
+ * synchronizes `stream`, reads and clears the word, and returns CIDER_OK or
+ * CIDER_ERR_TIMEOUT (CIDER_ERR_CUDA if the synchronization itself fails). */
+cider_status_t cider_check_device_error(void* stream);
+
+/* Test hook for the bounded-wait machinery: launches one CTA that waits on a
+ * barrier nothing will ever complete, giving up after `max_polls` polls.
+ * Returns the launch status; the timeout itself is reported by a following
+ * cider_check_device_error. */
+cider_status_t cider_debug_wait_timeout(int64_t max_polls, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CIDER_H */

@@ -1,0 +1,178 @@
+"""GPU parity of the integer GEMM paths (small-M GEMV and tensor-core GEMM)
+against the oracle.
+
+* int32 accumulators (per channel and per group): bit-exact, including
+  adversarial inputs whose sums exceed 2^24 (the fp32 significand) and mixes
+  of large and small products;
+* fp16 outputs: per channel bit-exact (same operation order as the oracle),
+  per group within |y - y_ref| <= 2e-3 max|y_ref| + 1 ulp;
+* the pre-quantized entry points give the same bits as the fused ones;
+* at the benchmark's full sizes, sampled rows against the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.parity_util import (assert_bits_equal, assert_fp16_close, require_gpu, to_dev,
+                               to_host)
+from w4a8_quantized_linear_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cider():
+    return require_gpu()
+
+
+def make_weights(N, K, gs, bits, seed):
+    W = inputs.weights(N, K, seed=seed)
+    if bits == 8:
+        qw, sw = oracle.quantize_weight_int8(W, gs)
+        return qw, qw, sw
+    q4, sw = oracle.quantize_weight_int4(W, gs)
+    return oracle.pack_int4(q4), q4, sw
+
+
+def run_acc(cider, qa, qw_dev_arr, gs, bits):
+    fn = cider.cider_w8a8_accumulators if bits == 8 else cider.cider_w4a8_accumulators
+    return to_host(fn(to_dev(qa), to_dev(qw_dev_arr), gs))
+
+
+def run_linear(cider, x, qw_dev_arr, sw, gs, bits):
+    fn = cider.cider_w8a8_linear if bits == 8 else cider.cider_w4a8_linear
+    return to_host(fn(to_dev(x), to_dev(qw_dev_arr), to_dev(sw), gs))
+
+
+SHAPES = [  # (M, N, K): GEMV bucket (M <= 16) and GEMM tiles with ragged edges
+    (1, 8, 128), (1, 136, 2560), (3, 64, 544), (5, 256, 1024), (16, 200, 2048),
+    (17, 136, 128), (64, 256, 576), (128, 128, 2560), (130, 264, 1088), (300, 200, 2048),
+    (257, 384, 4096),
+]
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("gs", [0, 64, 128])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_accumulators_bit_exact(cider, M, N, K, gs, bits):
+    if gs and K % gs:
+        pytest.skip("K not a multiple of the group size")
+    x = inputs.activations(M, K, seed=M + 3)
+    qa, _ = oracle.quantize_act(x)
+    qw_dev, qw_vals, _ = make_weights(N, K, gs, bits, seed=N + K)
+    acc = run_acc(cider, qa, qw_dev, gs, bits)
+    assert_bits_equal(acc, oracle.gemm_acc(qa, qw_vals, gs), f"acc M={M} N={N} K={K} gs={gs}")
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("M", [4, 160])
+def test_accumulators_exact_beyond_fp32_significand(cider, M, bits):
+    """All codes at the extreme: |acc| = 16129 K (8-bit) reaches 4.1e7 > 2^24
+    at K = 2560; plus rows mixing large products with +-1 products."""
+    N, K = 136, 2560
+    qa = np.full((M, K), 127, np.int8)
+    qa[1::2] = -127
+    qa[2, :] = 1
+    qa[3, 511::512] = 1                      # small terms right after a full chunk of big ones
+    if bits == 8:
+        qw_vals = np.full((N, K), 127, np.int8)
+        qw_vals[5, ::3] = -1
+        qw_vals[6, 1::2] = 1
+        qw_dev = qw_vals
+    else:
+        qw_vals = np.full((N, K), -8, np.int8)
+        qw_vals[5, ::3] = 7
+        qw_vals[6, 1::2] = 1
+        qw_dev = oracle.pack_int4(qw_vals)
+    for gs in (0, 64, 128):
+        acc = run_acc(cider, qa, qw_dev, gs, bits)
+        assert_bits_equal(acc, oracle.gemm_acc(qa, qw_vals, gs), f"extreme acc gs={gs}")
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("gs", [0, 64, 128])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_linear_matches_oracle(cider, M, N, K, gs, bits):
+    if gs and K % gs:
+        pytest.skip("K not a multiple of the group size")
+    x = inputs.activations(M, K, seed=M + 5)
+    qw_dev, qw_vals, sw = make_weights(N, K, gs, bits, seed=N + K + 1)
+    y = run_linear(cider, x, qw_dev, sw, gs, bits)
+    yref = oracle.linear(x, qw_vals, sw, gs)
+    if gs == 0:
+        assert_bits_equal(y, yref, f"y per-channel M={M} N={N} K={K}")
+    else:
+        assert_fp16_close(y, yref, f"y per-group M={M} N={N} K={K} gs={gs}")
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("gs", [0, 128])
+@pytest.mark.parametrize("M", [7, 200])
+def test_prequant_equals_fused(cider, M, gs, bits):
+    N, K = 264, 1024
+    x = inputs.activations(M, K, seed=21)
+    qw_dev, _, sw = make_weights(N, K, gs, bits, seed=22)
+    xd = to_dev(x)
+    qa, sa = cider.cider_quantize_act(xd)
+    fn_pre = cider.cider_w8a8_linear_prequant if bits == 8 else cider.cider_w4a8_linear_prequant
+    y_pre = to_host(fn_pre(qa, sa, to_dev(qw_dev), to_dev(sw), gs))
+    y = run_linear(cider, x, qw_dev, sw, gs, bits)
+    assert_bits_equal(y_pre, y, "prequant vs fused")
+
+
+def test_zero_activation_rows_give_zero(cider):
+    M, N, K = 130, 136, 512
+    x = inputs.activations(M, K, seed=30)
+    x[::3] = 0
+    qw_dev, qw_vals, sw = make_weights(N, K, 0, 8, seed=31)
+    y = run_linear(cider, x, qw_dev, sw, 0, 8)
+    assert not np.any(y[::3].astype(np.float32))
+    assert_bits_equal(y, oracle.linear(x, qw_vals, sw, 0), "zero rows")
+
+
+# Full-size workloads: sampled rows against the oracle (rows are independent,
+# so a row subset of the oracle is exact).
+FULL = [
+    # (M, N, K, gs, bits)
+    (4096, 10240, 2560, 0, 8),      # benchmark headline
+    (8192, 2560, 10240, 0, 8),
+    (4096, 10240, 2560, 128, 8),
+    (4096, 10240, 2560, 64, 8),
+    (4096, 10240, 2560, 128, 4),
+    (3455, 6144, 2048, 0, 8),       # Qwen3-2B-shaped gate/up at the longest prefill
+    (4096, 12288, 4096, 128, 4),    # Qwen3-8B-shaped gate/up
+    (1, 10240, 2560, 0, 8),
+    (16, 2560, 10240, 128, 4),
+    (1, 4096, 12288, 128, 8),       # Qwen3-8B-shaped down projection, decode
+]
+
+
+@pytest.mark.parametrize("M,N,K,gs,bits", FULL)
+def test_full_size_sampled_rows(cider, M, N, K, gs, bits):
+    x = inputs.activations(M, K, seed=0)
+    qw_dev, qw_vals, sw = make_weights(N, K, gs, bits, seed=1)
+    y = run_linear(cider, x, qw_dev, sw, gs, bits)
+    rng = np.random.default_rng(M + N)
+    rows = sorted(set([0, M - 1, M // 2] + list(rng.integers(0, M, 5))))
+    yref = oracle.linear(x, qw_vals, sw, gs, rows=rows, threads=8)
+    if gs == 0:
+        assert_bits_equal(y[rows], yref, f"full-size rows M={M} N={N} K={K}")
+    else:
+        assert_fp16_close(y[rows], yref, f"full-size rows M={M} N={N} K={K} gs={gs}")
+
+
+def test_no_device_error_left(cider):
+    assert cider.cider_check_device_error() == 0
+
+
+def test_bounded_wait_reports_timeout(cider):
+    """A kernel waiting on a barrier nothing completes gives up after the poll
+    limit, sets the device error word, and the context stays usable."""
+    assert cider.cider_debug_wait_timeout(1000) == 0
+    assert cider.cider_check_device_error() == 5
+    assert cider.cider_check_device_error() == 0
+    x = torch.zeros((2, 64), dtype=torch.float16, device="cuda")
+    qa, sa = cider.cider_quantize_act(x)
+    torch.cuda.synchronize()
+    assert float(sa.sum()) == 2.0

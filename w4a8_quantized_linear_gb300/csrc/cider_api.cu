@@ -1,0 +1,411 @@
+// cider_api.cu -- the C ABI declared in include/cider.h: argument checks,
+// device check, scratch memory from a per-device stream-ordered pool, and
+// the dispatch by M between the small-M GEMV and the tensor-core GEMM.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "cider.h"
+#include "cider_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxK = 131072;  // keeps |acc| <= 16129 * K below 2^31
+constexpr int64_t kMaxDim = 2147483647;
+
+struct DeviceInfo {
+  std::atomic<int> state{0};  // 0 unknown, 1 supported, 2 unsupported
+  int num_sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+std::mutex g_pool_mu;
+cudaMemPool_t g_pool[kMaxDevices] = {};
+
+bool force_unsupported() {
+  const char* v = getenv("CIDER_FORCE_UNSUPPORTED");
+  return v != nullptr && v[0] == '1';
+}
+
+// Supported = compute capability 10.3 (GB300).  Caches the SM count.
+cider_status_t check_device(int* dev_out, int* num_sms) {
+  if (force_unsupported()) return CIDER_ERR_UNSUPPORTED_DEVICE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return CIDER_ERR_UNSUPPORTED_DEVICE;
+  }
+  DeviceInfo& d = g_dev[dev];
+  int st = d.state.load(std::memory_order_acquire);
+  if (st == 0) {
+    int major = 0, minor = 0, sms = 0;
+    bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+              cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+              cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
+    if (!ok) cudaGetLastError();
+    ok = ok && major == 10 && minor == 3 && sms > 0;
+    d.num_sms = sms;
+    st = ok ? 1 : 2;
+    d.state.store(st, std::memory_order_release);
+  }
+  if (st != 1) return CIDER_ERR_UNSUPPORTED_DEVICE;
+  if (dev_out) *dev_out = dev;
+  if (num_sms) *num_sms = d.num_sms;
+  return CIDER_OK;
+}
+
+cudaError_t get_pool(int dev, cudaMemPool_t* pool) {
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  if (!g_pool[dev]) {
+    cudaMemPoolProps props;
+    memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t p;
+    cudaError_t e = cudaMemPoolCreate(&p, &props);
+    if (e != cudaSuccess) return e;
+    uint64_t keep = UINT64_MAX;  // keep freed blocks for reuse by later calls
+    e = cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) {
+      cudaMemPoolDestroy(p);
+      return e;
+    }
+    g_pool[dev] = p;
+  }
+  *pool = g_pool[dev];
+  return cudaSuccess;
+}
+
+// Scratch for one call, allocated and freed in stream order.
+struct Scratch {
+  void* ptr = nullptr;
+  cudaStream_t st = nullptr;
+  ~Scratch() {
+    if (ptr) cudaFreeAsync(ptr, st);
+  }
+};
+
+cudaError_t scratch_alloc(Scratch& s, int dev, size_t bytes, cudaStream_t st) {
+  cudaMemPool_t pool;
+  cudaError_t e = get_pool(dev, &pool);
+  if (e != cudaSuccess) return e;
+  s.st = st;
+  return cudaMallocFromPoolAsync(&s.ptr, bytes, pool, st);
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+cider_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return CIDER_OK;
+  cudaGetLastError();  // clear a sticky launch error so later calls start clean
+  return CIDER_ERR_CUDA;
+}
+
+bool valid_k(int64_t K) { return K >= 32 && K % 32 == 0 && K <= kMaxK; }
+
+// Granularity / group size rules shared by the linears.
+bool valid_grouping(int granularity, int group_size, int64_t K) {
+  if (granularity == CIDER_PER_CHANNEL) return group_size == 0;
+  if (granularity == CIDER_PER_GROUP)
+    return (group_size == 64 || group_size == 128) && K % group_size == 0;
+  return false;
+}
+
+thread_local cudaEvent_t t_ev_start = nullptr;
+thread_local cudaEvent_t t_ev_stop = nullptr;
+
+// Record the caller's timing events around one GEMM launch (if set).
+template <typename F>
+cudaError_t timed_launch(cudaStream_t st, F&& launch) {
+  const bool timed = t_ev_start != nullptr && t_ev_stop != nullptr;
+  if (timed) {
+    cudaError_t e = cudaEventRecord(t_ev_start, st);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = launch();
+  if (e != cudaSuccess) return e;
+  if (timed) return cudaEventRecord(t_ev_stop, st);
+  return cudaSuccess;
+}
+
+struct LinearArgs {
+  const void* x = nullptr;  // fp16 activations (or null for the prequant forms)
+  const int8_t* qa = nullptr;
+  const float* sa = nullptr;
+  int64_t M = 0, N = 0, K = 0;
+  const void* w = nullptr;
+  bool int4 = false;
+  const float* sw = nullptr;
+  int granularity = 0, group_size = 0;
+  void* y = nullptr;
+  int32_t* acc = nullptr;
+  int mode = cider::kEpiY;
+  cudaStream_t st = nullptr;
+};
+
+cider_status_t validate_linear(const LinearArgs& a) {
+  if (a.M < 0 || a.N < 0 || a.K < 0) return CIDER_ERR_INVALID_ARGUMENT;
+  if (a.M > kMaxDim || a.N > kMaxDim) return CIDER_ERR_INVALID_ARGUMENT;
+  const bool prequant = a.x == nullptr;
+  if (prequant ? (!a.qa || (a.mode == cider::kEpiY && !a.sa)) : false)
+    return CIDER_ERR_INVALID_ARGUMENT;
+  if (!a.w) return CIDER_ERR_INVALID_ARGUMENT;
+  if (a.mode == cider::kEpiY && (!a.sw || !a.y)) return CIDER_ERR_INVALID_ARGUMENT;
+  if (a.mode == cider::kEpiAcc && !a.acc) return CIDER_ERR_INVALID_ARGUMENT;
+  if (!valid_k(a.K) || a.N % 8 != 0) return CIDER_ERR_INVALID_ARGUMENT;
+  if (a.mode == cider::kEpiY) {
+    if (!valid_grouping(a.granularity, a.group_size, a.K)) return CIDER_ERR_INVALID_ARGUMENT;
+  } else {
+    if (!(a.group_size == 0 || ((a.group_size == 64 || a.group_size == 128) && a.K % a.group_size == 0)))
+      return CIDER_ERR_INVALID_ARGUMENT;
+  }
+  if ((a.x && !aligned(a.x, 16)) || (a.qa && !aligned(a.qa, 16)) || !aligned(a.w, 16) ||
+      (a.y && !aligned(a.y, 16)))
+    return CIDER_ERR_MISALIGNED;
+  if ((a.sa && !aligned(a.sa, 4)) || (a.sw && !aligned(a.sw, 4)) || (a.acc && !aligned(a.acc, 4)))
+    return CIDER_ERR_MISALIGNED;
+  return CIDER_OK;
+}
+
+cider_status_t run_linear(const LinearArgs& a) {
+  if (a.M == 0 || a.N == 0) return CIDER_OK;
+  cider_status_t s = validate_linear(a);
+  if (s != CIDER_OK) return s;
+  int dev = 0, sms = 0;
+  s = check_device(&dev, &sms);
+  if (s != CIDER_OK) return s;
+  const uint8_t* w = static_cast<const uint8_t*>(a.w);
+  __half* y = static_cast<__half*>(a.y);
+  const int gs = a.group_size;
+  Scratch scratch;
+  if (cider::gemv_fits(a.M, a.K)) {
+    const int8_t* qa = a.qa;
+    const float* sa = a.sa;
+    if (a.x) {
+      const size_t qbytes = round_up(static_cast<size_t>(a.M * a.K), 256);
+      cudaError_t e = scratch_alloc(scratch, dev, qbytes + round_up(4 * a.M, 256), a.st);
+      if (e != cudaSuccess) return cuda_status(e);
+      int8_t* q = static_cast<int8_t*>(scratch.ptr);
+      float* sscr = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch.ptr) + qbytes);
+      e = cider::launch_quant_act_s8(static_cast<const __half*>(a.x), a.M, a.K, q, sscr, a.st);
+      if (e != cudaSuccess) return cuda_status(e);
+      qa = q;
+      sa = sscr;
+    }
+    return cuda_status(timed_launch(a.st, [&] {
+      return cider::launch_gemv(qa, sa, a.M, a.N, a.K, w, a.int4, a.sw, gs, a.mode, y, a.acc, sms,
+                                a.st);
+    }));
+  }
+  // tensor-core path: activation codes as fp16 integers
+  const size_t qbytes = round_up(static_cast<size_t>(a.M * a.K) * 2, 256);
+  cudaError_t e = scratch_alloc(scratch, dev, qbytes + round_up(4 * a.M, 256), a.st);
+  if (e != cudaSuccess) return cuda_status(e);
+  __half* q16 = static_cast<__half*>(scratch.ptr);
+  const float* sa = a.sa;
+  if (a.x) {
+    float* sscr = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch.ptr) + qbytes);
+    e = cider::launch_quant_act_f16(static_cast<const __half*>(a.x), a.M, a.K, q16, sscr, a.st);
+    sa = sscr;
+  } else {
+    e = cider::launch_codes_s8_to_f16(a.qa, a.M * a.K, q16, a.st);
+  }
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(timed_launch(a.st, [&] {
+    return cider::launch_gemm_tc(q16, sa, a.M, a.N, a.K, w, a.int4, a.sw, gs, a.mode, y, a.acc,
+                                 sms, a.st);
+  }));
+}
+
+template <typename F>
+cider_status_t guarded(F&& f) {
+  try {
+    return f();
+  } catch (...) {
+    return CIDER_ERR_CUDA;
+  }
+}
+
+cider_status_t quantize_weight(const float* w, int64_t N, int64_t K, int group_size, void* q,
+                               float* sw, bool int4, void* stream) {
+  if (N == 0) return CIDER_OK;
+  if (N < 0 || N > kMaxDim || !w || !q || !sw || !valid_k(K)) return CIDER_ERR_INVALID_ARGUMENT;
+  if (!(group_size == 0 || ((group_size == 64 || group_size == 128) && K % group_size == 0)))
+    return CIDER_ERR_INVALID_ARGUMENT;
+  if (!aligned(w, 16) || !aligned(q, 16)) return CIDER_ERR_MISALIGNED;
+  if (!aligned(sw, 4)) return CIDER_ERR_MISALIGNED;
+  cider_status_t s = check_device(nullptr, nullptr);
+  if (s != CIDER_OK) return s;
+  return cuda_status(cider::launch_quant_weight(w, N, K, group_size, int4,
+                                                static_cast<uint8_t*>(q), sw,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int cider_version(void) { return 100; }
+
+int cider_is_available(void) { return check_device(nullptr, nullptr) == CIDER_OK ? 1 : 0; }
+
+const char* cider_status_string(int status) {
+  switch (status) {
+    case CIDER_OK: return "CIDER_OK";
+    case CIDER_ERR_INVALID_ARGUMENT: return "CIDER_ERR_INVALID_ARGUMENT: bad size, pointer or mode";
+    case CIDER_ERR_MISALIGNED: return "CIDER_ERR_MISALIGNED: a pointer is not aligned as required";
+    case CIDER_ERR_UNSUPPORTED_DEVICE: return "CIDER_ERR_UNSUPPORTED_DEVICE: current device is not sm_103";
+    case CIDER_ERR_CUDA: return "CIDER_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+    case CIDER_ERR_TIMEOUT: return "CIDER_ERR_TIMEOUT: a bounded wait inside a kernel gave up";
+    default: return "unknown cider status";
+  }
+}
+
+cider_status_t cider_quantize_act(const void* x, int64_t M, int64_t K, int8_t* qa, float* sa,
+                                  void* stream) {
+  return guarded([&]() -> cider_status_t {
+    if (M == 0) return CIDER_OK;
+    if (M < 0 || M > kMaxDim || !x || !qa || !sa || !valid_k(K)) return CIDER_ERR_INVALID_ARGUMENT;
+    if (!aligned(x, 16) || !aligned(qa, 16)) return CIDER_ERR_MISALIGNED;
+    if (!aligned(sa, 4)) return CIDER_ERR_MISALIGNED;
+    cider_status_t s = check_device(nullptr, nullptr);
+    if (s != CIDER_OK) return s;
+    return cuda_status(cider::launch_quant_act_s8(static_cast<const __half*>(x), M, K, qa, sa,
+                                                  static_cast<cudaStream_t>(stream)));
+  });
+}
+
+cider_status_t cider_quantize_weight_int8(const float* w, int64_t N, int64_t K, int group_size,
+                                          int8_t* qw, float* sw, void* stream) {
+  return guarded([&] { return quantize_weight(w, N, K, group_size, qw, sw, false, stream); });
+}
+
+cider_status_t cider_quantize_weight_int4(const float* w, int64_t N, int64_t K, int group_size,
+                                          uint8_t* qw_packed, float* sw, void* stream) {
+  return guarded([&] { return quantize_weight(w, N, K, group_size, qw_packed, sw, true, stream); });
+}
+
+static cider_status_t linear_entry(const void* x, const int8_t* qa, const float* sa, int64_t M,
+                                   int64_t N, int64_t K, const void* w, bool int4, const float* sw,
+                                   int granularity, int group_size, void* y, void* stream) {
+  return guarded([&] {
+    LinearArgs a;
+    a.x = x;
+    a.qa = qa;
+    a.sa = sa;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.w = w;
+    a.int4 = int4;
+    a.sw = sw;
+    a.granularity = granularity;
+    a.group_size = group_size;
+    a.y = y;
+    a.mode = cider::kEpiY;
+    a.st = static_cast<cudaStream_t>(stream);
+    if (M == 0 || N == 0) return CIDER_OK;
+    if (!x && !qa) return CIDER_ERR_INVALID_ARGUMENT;
+    return run_linear(a);
+  });
+}
+
+cider_status_t cider_w8a8_linear(const void* x, int64_t M, int64_t N, int64_t K, const int8_t* qw,
+                                 const float* sw, int granularity, int group_size, void* y,
+                                 void* stream) {
+  if (x == nullptr && M != 0 && N != 0) return CIDER_ERR_INVALID_ARGUMENT;
+  return linear_entry(x, nullptr, nullptr, M, N, K, qw, false, sw, granularity, group_size, y, stream);
+}
+
+cider_status_t cider_w4a8_linear(const void* x, int64_t M, int64_t N, int64_t K,
+                                 const uint8_t* qw_packed, const float* sw, int granularity,
+                                 int group_size, void* y, void* stream) {
+  if (x == nullptr && M != 0 && N != 0) return CIDER_ERR_INVALID_ARGUMENT;
+  return linear_entry(x, nullptr, nullptr, M, N, K, qw_packed, true, sw, granularity, group_size, y,
+                      stream);
+}
+
+cider_status_t cider_w8a8_linear_prequant(const int8_t* qa, const float* sa, int64_t M, int64_t N,
+                                          int64_t K, const int8_t* qw, const float* sw,
+                                          int granularity, int group_size, void* y, void* stream) {
+  if ((qa == nullptr || sa == nullptr) && M != 0 && N != 0) return CIDER_ERR_INVALID_ARGUMENT;
+  return linear_entry(nullptr, qa, sa, M, N, K, qw, false, sw, granularity, group_size, y, stream);
+}
+
+cider_status_t cider_w4a8_linear_prequant(const int8_t* qa, const float* sa, int64_t M, int64_t N,
+                                          int64_t K, const uint8_t* qw_packed, const float* sw,
+                                          int granularity, int group_size, void* y, void* stream) {
+  if ((qa == nullptr || sa == nullptr) && M != 0 && N != 0) return CIDER_ERR_INVALID_ARGUMENT;
+  return linear_entry(nullptr, qa, sa, M, N, K, qw_packed, true, sw, granularity, group_size, y,
+                      stream);
+}
+
+static cider_status_t acc_entry(const int8_t* qa, int64_t M, int64_t N, int64_t K, const void* w,
+                                bool int4, int group_size, int32_t* acc, void* stream) {
+  return guarded([&] {
+    if (M != 0 && N != 0 && !qa) return CIDER_ERR_INVALID_ARGUMENT;
+    LinearArgs a;
+    a.qa = qa;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.w = w;
+    a.int4 = int4;
+    a.group_size = group_size;
+    a.acc = acc;
+    a.mode = cider::kEpiAcc;
+    a.st = static_cast<cudaStream_t>(stream);
+    return run_linear(a);
+  });
+}
+
+cider_status_t cider_w8a8_accumulators(const int8_t* qa, int64_t M, int64_t N, int64_t K,
+                                       const int8_t* qw, int group_size, int32_t* acc,
+                                       void* stream) {
+  return acc_entry(qa, M, N, K, qw, false, group_size, acc, stream);
+}
+
+cider_status_t cider_w4a8_accumulators(const int8_t* qa, int64_t M, int64_t N, int64_t K,
+                                       const uint8_t* qw_packed, int group_size, int32_t* acc,
+                                       void* stream) {
+  return acc_entry(qa, M, N, K, qw_packed, true, group_size, acc, stream);
+}
+
+cider_status_t cider_set_gemm_events(void* ev_start, void* ev_stop) {
+  t_ev_start = static_cast<cudaEvent_t>(ev_start);
+  t_ev_stop = static_cast<cudaEvent_t>(ev_stop);
+  return CIDER_OK;
+}
+
+cider_status_t cider_check_device_error(void* stream) {
+  return guarded([&] {
+    cider_status_t s = check_device(nullptr, nullptr);
+    if (s != CIDER_OK) return s;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return cuda_status(cudaErrorUnknown);
+    int v = 0;
+    if (cider::read_and_clear_device_error(&v) != cudaSuccess) return cuda_status(cudaErrorUnknown);
+    return v ? CIDER_ERR_TIMEOUT : CIDER_OK;
+  });
+}
+
+cider_status_t cider_debug_wait_timeout(int64_t max_polls, void* stream) {
+  return guarded([&] {
+    if (max_polls < 1) return CIDER_ERR_INVALID_ARGUMENT;
+    cider_status_t s = check_device(nullptr, nullptr);
+    if (s != CIDER_OK) return s;
+    return cuda_status(cider::launch_debug_wait_timeout(max_polls, static_cast<cudaStream_t>(stream)));
+  });
+}
+
+}  // extern "C"

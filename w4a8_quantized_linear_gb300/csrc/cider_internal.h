@@ -1,0 +1,57 @@
+// cider_internal.h -- launchers shared between the translation units of the
+// library (not part of the public ABI).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+namespace cider {
+
+// Raise a kernel's dynamic shared memory limit once per device (bit d of
+// `done` records device d).
+inline cudaError_t ensure_max_dynamic_smem(const void* kern, int bytes,
+                                           std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev < 64) ? (uint64_t{1} << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// Epilogue kinds of the integer GEMM / GEMV main loops.
+enum EpiMode : int {
+  kEpiY = 0,    // dequantize and store fp16 y [M, N]
+  kEpiAcc = 1,  // store the exact int32 accumulators [M, N, G]
+};
+
+// quant.cu
+cudaError_t launch_quant_act_s8(const __half* x, int64_t M, int64_t K, int8_t* q, float* sa,
+                                cudaStream_t st);
+cudaError_t launch_quant_act_f16(const __half* x, int64_t M, int64_t K, __half* q, float* sa,
+                                 cudaStream_t st);
+cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int group_size, bool int4,
+                                uint8_t* q, float* sw, cudaStream_t st);
+cudaError_t launch_codes_s8_to_f16(const int8_t* qa, int64_t count, __half* out, cudaStream_t st);
+
+// gemv.cu: small-M weight-streaming path.  qa int8 [M, K] (M <= 16).
+// group_size 0 = per channel.  Exactly one of y / acc is used (by mode).
+bool gemv_fits(int64_t M, int64_t K);
+cudaError_t launch_gemv(const int8_t* qa, const float* sa, int64_t M, int64_t N, int64_t K,
+                        const uint8_t* w, bool int4, const float* sw, int group_size, int mode,
+                        __half* y, int32_t* acc, int num_sms, cudaStream_t st);
+
+// gemm_tc.cu: tensor-core path.  qa16 holds the activation codes as fp16
+// integers [M, K].
+cudaError_t launch_gemm_tc(const __half* qa16, const float* sa, int64_t M, int64_t N, int64_t K,
+                           const uint8_t* w, bool int4, const float* sw, int group_size,
+                           int mode, __half* y, int32_t* acc, int num_sms, cudaStream_t st);
+cudaError_t read_and_clear_device_error(int* value);
+cudaError_t launch_debug_wait_timeout(int64_t max_polls, cudaStream_t st);
+
+}  // namespace cider

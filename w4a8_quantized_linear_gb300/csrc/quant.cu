@@ -1,0 +1,250 @@
+// quant.cu -- per-token activation quantization and offline weight
+// quantization kernels.
+//
+// Activation quantization follows the Cider README (page "cider"),
+// "Architecture / Metal kernel pipeline", step quantize_per_token, and the
+// "Quantization" table row "Activations: symmetric INT8, per token":
+//   s_a = max_k |x[m,k]| / 127 (IEEE fp32 divide; 1 for an all-zero row),
+//   q   = clamp(rint(x / s_a), -127, 127) with ties to even.
+// Weight quantization follows "Notes" (min-max scales) and the "Quantization"
+// table (INT8 per channel or per group of 64 / 128; INT4 for W4A8, "Modes").
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "cider_device.cuh"
+#include "cider_internal.h"
+
+namespace cider {
+namespace {
+
+constexpr int kQuantThreads = 128;
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float block_max_128(float v, float* red) {
+  v = warp_max(v);
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[warp] = v;
+  __syncthreads();
+  v = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  return v;
+}
+
+__device__ __forceinline__ float quant_code(float x, float s) {
+  float r = rintf(__fdiv_rn(x, s));
+  return fminf(fmaxf(r, -127.0f), 127.0f);
+}
+
+// Eight fp16 values -> eight codes, stored as int8 (8 bytes) or as fp16
+// integers (16 bytes; exact, the operand format of the tensor-core GEMM).
+__device__ __forceinline__ void store_codes(int8_t* q, int64_t off, const uint4& v, float s) {
+  const __half2* h = reinterpret_cast<const __half2*>(&v);
+  uint32_t w[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    uint32_t b = 0;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float2 f = __half22float2(h[2 * j + e]);
+      int c0 = static_cast<int>(quant_code(f.x, s));
+      int c1 = static_cast<int>(quant_code(f.y, s));
+      b |= (static_cast<uint32_t>(c0 & 0xFF) << (16 * e)) |
+           (static_cast<uint32_t>(c1 & 0xFF) << (16 * e + 8));
+    }
+    w[j] = b;
+  }
+  *reinterpret_cast<uint2*>(q + off) = make_uint2(w[0], w[1]);
+}
+__device__ __forceinline__ void store_codes(__half* q, int64_t off, const uint4& v, float s) {
+  const __half2* h = reinterpret_cast<const __half2*>(&v);
+  uint4 o;
+  uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float2 f = __half22float2(h[j]);
+    __half2 r = __floats2half2_rn(quant_code(f.x, s), quant_code(f.y, s));
+    ow[j] = *reinterpret_cast<uint32_t*>(&r);
+  }
+  *reinterpret_cast<uint4*>(q + off) = o;
+}
+
+// One CTA of 128 threads per row; the row stays in registers between the
+// amax pass and the quantization pass (VPT 16-byte vectors per thread).
+template <typename OutT, int VPT>
+__global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const __half* __restrict__ x,
+                                                                  int64_t K, OutT* __restrict__ q,
+                                                                  float* __restrict__ sa) {
+  __shared__ float red[4];
+  const int64_t m = blockIdx.x;
+  const uint4* row = reinterpret_cast<const uint4*>(x + m * K);
+  const int nvec = static_cast<int>(K >> 3);
+  uint4 v[VPT];
+  __half2 amax2 = __float2half2_rn(0.0f);
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = threadIdx.x + i * kQuantThreads;
+    if (idx < nvec) {
+      v[i] = ld_stream_v4(row + idx);
+      const __half2* h = reinterpret_cast<const __half2*>(&v[i]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) amax2 = __hmax2(amax2, __habs2(h[j]));
+    }
+  }
+  float amax = fmaxf(__low2float(amax2), __high2float(amax2));
+  amax = block_max_128(amax, red);
+  const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
+  if (threadIdx.x == 0) sa[m] = s;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = threadIdx.x + i * kQuantThreads;
+    if (idx < nvec) store_codes(q, m * K + static_cast<int64_t>(idx) * 8, v[i], s);
+  }
+}
+
+// Rows longer than the register-resident variants: two passes over global
+// memory (the second pass hits L1/L2).
+template <typename OutT>
+__global__ void __launch_bounds__(kQuantThreads) quant_act_long_kernel(const __half* __restrict__ x,
+                                                                       int64_t K,
+                                                                       OutT* __restrict__ q,
+                                                                       float* __restrict__ sa) {
+  __shared__ float red[4];
+  const int64_t m = blockIdx.x;
+  const uint4* row = reinterpret_cast<const uint4*>(x + m * K);
+  const int64_t nvec = K >> 3;
+  __half2 amax2 = __float2half2_rn(0.0f);
+  for (int64_t idx = threadIdx.x; idx < nvec; idx += kQuantThreads) {
+    uint4 v = row[idx];
+    const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) amax2 = __hmax2(amax2, __habs2(h[j]));
+  }
+  float amax = fmaxf(__low2float(amax2), __high2float(amax2));
+  amax = block_max_128(amax, red);
+  const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
+  if (threadIdx.x == 0) sa[m] = s;
+  for (int64_t idx = threadIdx.x; idx < nvec; idx += kQuantThreads)
+    store_codes(q, m * K + idx * 8, row[idx], s);
+}
+
+template <typename OutT>
+cudaError_t launch_quant_act(const __half* x, int64_t M, int64_t K, OutT* q, float* sa,
+                             cudaStream_t st) {
+  const int64_t nvec = K / 8;
+  const int vpt = static_cast<int>((nvec + kQuantThreads - 1) / kQuantThreads);
+  const dim3 grid(static_cast<unsigned>(M));
+  if (vpt <= 1)
+    quant_act_kernel<OutT, 1><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+  else if (vpt <= 2)
+    quant_act_kernel<OutT, 2><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+  else if (vpt <= 3)
+    quant_act_kernel<OutT, 3><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+  else if (vpt <= 4)
+    quant_act_kernel<OutT, 4><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+  else if (vpt <= 6)
+    quant_act_kernel<OutT, 6><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+  else if (vpt <= 8)
+    quant_act_kernel<OutT, 8><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+  else if (vpt <= 12)
+    quant_act_kernel<OutT, 12><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+  else if (vpt <= 16)
+    quant_act_kernel<OutT, 16><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+  else
+    quant_act_long_kernel<OutT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- weights
+// One warp per (row, block): block = the whole row (per channel) or
+// group_size consecutive elements (per group).  Each lane takes element
+// pairs (2j, 2j+1) so the INT4 variant writes whole packed bytes.
+template <bool INT4>
+__global__ void __launch_bounds__(256) quant_weight_kernel(const float* __restrict__ w, int64_t N,
+                                                           int64_t K, int64_t bs, int64_t G,
+                                                           uint8_t* __restrict__ q,
+                                                           float* __restrict__ sw) {
+  const int lane = threadIdx.x & 31;
+  const int64_t blk = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (blk >= N * G) return;
+  const int64_t n = blk / G, g = blk % G;
+  const float2* src = reinterpret_cast<const float2*>(w + n * K + g * bs);
+  const int64_t npairs = bs / 2;
+  float amax = 0.0f;
+  for (int64_t j = lane; j < npairs; j += 32) {
+    float2 v = src[j];
+    amax = fmaxf(amax, fmaxf(fabsf(v.x), fabsf(v.y)));
+  }
+  amax = warp_max(amax);
+  const float qdiv = INT4 ? 7.0f : 127.0f;
+  const float qmin = INT4 ? -8.0f : -127.0f;
+  const float qmax = INT4 ? 7.0f : 127.0f;
+  const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, qdiv);
+  if (lane == 0) sw[n * G + g] = s;
+  for (int64_t j = lane; j < npairs; j += 32) {
+    float2 v = src[j];
+    int c0 = static_cast<int>(fminf(fmaxf(rintf(__fdiv_rn(v.x, s)), qmin), qmax));
+    int c1 = static_cast<int>(fminf(fmaxf(rintf(__fdiv_rn(v.y, s)), qmin), qmax));
+    if (INT4) {
+      q[n * (K / 2) + g * (bs / 2) + j] =
+          static_cast<uint8_t>((c0 & 0xF) | ((c1 & 0xF) << 4));
+    } else {
+      uint8_t* dst = q + n * K + g * bs + 2 * j;
+      *reinterpret_cast<uint16_t*>(dst) =
+          static_cast<uint16_t>((c0 & 0xFF) | ((c1 & 0xFF) << 8));
+    }
+  }
+}
+
+// int8 codes -> the same codes as fp16 integers (exact), 16 per thread.
+__global__ void __launch_bounds__(256) codes_s8_to_f16_kernel(const int8_t* __restrict__ qa,
+                                                              int64_t n16,
+                                                              __half* __restrict__ out) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n16) return;
+  const uint4 v = ld_stream_v4(qa + i * 16);
+  uint4 o0, o1;
+  s8x4_to_h2x2(v.x, o0.x, o0.y);
+  s8x4_to_h2x2(v.y, o0.z, o0.w);
+  s8x4_to_h2x2(v.z, o1.x, o1.y);
+  s8x4_to_h2x2(v.w, o1.z, o1.w);
+  uint4* dst = reinterpret_cast<uint4*>(out + i * 16);
+  dst[0] = o0;
+  dst[1] = o1;
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act_s8(const __half* x, int64_t M, int64_t K, int8_t* q, float* sa,
+                                cudaStream_t st) {
+  return launch_quant_act<int8_t>(x, M, K, q, sa, st);
+}
+
+cudaError_t launch_quant_act_f16(const __half* x, int64_t M, int64_t K, __half* q, float* sa,
+                                 cudaStream_t st) {
+  return launch_quant_act<__half>(x, M, K, q, sa, st);
+}
+
+cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int group_size, bool int4,
+                                uint8_t* q, float* sw, cudaStream_t st) {
+  const int64_t bs = group_size > 0 ? group_size : K;
+  const int64_t G = K / bs;
+  const int64_t blocks = (N * G + 7) / 8;
+  if (int4)
+    quant_weight_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, st>>>(w, N, K, bs, G, q, sw);
+  else
+    quant_weight_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(w, N, K, bs, G, q, sw);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_codes_s8_to_f16(const int8_t* qa, int64_t count, __half* out, cudaStream_t st) {
+  const int64_t n16 = count / 16;
+  const int64_t blocks = (n16 + 255) / 256;
+  codes_s8_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(qa, n16, out);
+  return cudaGetLastError();
+}
+
+}  // namespace cider
