@@ -160,14 +160,17 @@ cider_status_t cider_w4a8_accumulators(const int8_t* qa, int64_t M, int64_t N,
                                        int group_size, int32_t* acc,
                                        void* stream);
 
-/* Optional timing hook for benchmarks.  When both events are non-NULL, every
- * later linear / accumulator call made from the calling host thread records
- * `ev_start` on its stream immediately before launching its integer-GEMM
- * kernel (the tensor-core GEMM, or the GEMV for M <= 16) and `ev_stop`
- * immediately after it, so cudaEventElapsedTime gives that kernel's device
- * time.  Pass NULL, NULL to stop.  The events are caller-owned cudaEvent_t
- * handles created with timing enabled.  Always returns CIDER_OK. */
-cider_status_t cider_set_gemm_events(void* ev_start, void* ev_stop);
+/* Kernel timing for benchmarks.  After cider_timing_begin(capacity), each of
+ * the next `capacity` linear / accumulator calls made from the calling host
+ * thread records a pair of CUDA events (created here, owned by the library)
+ * on its stream immediately before and after launching its integer-GEMM
+ * kernel (the tensor-core GEMM, or the GEMV for M <= 16).
+ * cider_timing_end waits for those events, writes the number of timed
+ * launches and their summed device time in milliseconds, releases the events
+ * and stops timing.  Returns CIDER_ERR_CUDA if an event call fails,
+ * CIDER_ERR_INVALID_ARGUMENT for capacity < 1 or NULL outputs. */
+cider_status_t cider_timing_begin(int64_t capacity);
+cider_status_t cider_timing_end(int64_t* count, double* total_ms);
 
 /* Device-side error word shared by the library's kernels on the current
  * device.  Every wait inside a kernel is bounded; a wait that runs out sets

@@ -129,3 +129,8 @@ def test_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(pkg, "LIB_PATH", "/nonexistent/libcider.so")
     with pytest.raises(RuntimeError, match="no fallback"):
         pkg.library()
+
+
+def test_timing_argument_checks(lib):
+    assert lib.cider_timing_begin(0) == INVALID
+    assert lib.cider_timing_end(None, None) == INVALID

@@ -176,3 +176,16 @@ def test_bounded_wait_reports_timeout(cider):
     qa, sa = cider.cider_quantize_act(x)
     torch.cuda.synchronize()
     assert float(sa.sum()) == 2.0
+
+
+def test_kernel_timing_facility(cider):
+    M, N, K = 256, 512, 1024
+    x = torch.from_numpy(inputs.activations(M, K, seed=3)).cuda()
+    qw, sw = cider.cider_quantize_weight_int8(torch.from_numpy(inputs.weights(N, K)).cuda(), 0)
+    cider.cider_timing_begin(2)
+    for _ in range(3):                     # the third call is beyond the capacity: untimed
+        cider.cider_w8a8_linear(x, qw, sw, 0)
+    n, ms = cider.cider_timing_end()
+    assert n == 2 and ms > 0.0
+    n, ms = cider.cider_timing_end()       # timing is off again
+    assert n == 0 and ms == 0.0

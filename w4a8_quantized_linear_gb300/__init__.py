@@ -55,7 +55,8 @@ def _declare(lib):
         "cider_w8a8_accumulators": ([p, i64, i64, i64, p, i32, p, p], i32),
         "cider_w4a8_accumulators": ([p, i64, i64, i64, p, i32, p, p], i32),
         "cider_check_device_error": ([p], i32),
-        "cider_set_gemm_events": ([p, p], i32),
+        "cider_timing_begin": ([i64], i32),
+        "cider_timing_end": ([ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)], i32),
         "cider_debug_wait_timeout": ([i64, p], i32),
     }
     for name, (args, res) in sig.items():
@@ -236,9 +237,15 @@ def cider_debug_wait_timeout(max_polls: int, device=None) -> int:
     return int(_load().cider_debug_wait_timeout(int(max_polls), ctypes.c_void_p(s.cuda_stream)))
 
 
-def cider_set_gemm_events(ev_start=None, ev_stop=None) -> None:
-    """Record two torch.cuda.Event (enable_timing=True) around the integer-GEMM
-    kernel of each following linear call from this thread; None, None stops."""
-    a = ctypes.c_void_p(ev_start.cuda_event) if ev_start is not None else None
-    b = ctypes.c_void_p(ev_stop.cuda_event) if ev_stop is not None else None
-    _check("cider_set_gemm_events", _load().cider_set_gemm_events(a, b))
+def cider_timing_begin(capacity: int) -> None:
+    """Time the integer-GEMM kernel of the next `capacity` linear calls made
+    from this thread (CUDA events recorded by the library around each launch)."""
+    _check("cider_timing_begin", _load().cider_timing_begin(int(capacity)))
+
+
+def cider_timing_end():
+    """-> (number of timed launches, their summed device time in ms)."""
+    n = ctypes.c_int64(0)
+    ms = ctypes.c_double(0.0)
+    _check("cider_timing_end", _load().cider_timing_end(ctypes.byref(n), ctypes.byref(ms)))
+    return int(n.value), float(ms.value)

@@ -9,6 +9,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "cider.h"
 #include "cider_internal.h"
@@ -121,20 +122,40 @@ bool valid_grouping(int granularity, int group_size, int64_t K) {
   return false;
 }
 
-thread_local cudaEvent_t t_ev_start = nullptr;
-thread_local cudaEvent_t t_ev_stop = nullptr;
+// Per-thread kernel timing (cider_timing_begin / cider_timing_end).
+struct KernelTimer {
+  std::vector<cudaEvent_t> ev;  // pairs: 2 i (before), 2 i + 1 (after)
+  int64_t used = 0;
+  bool on = false;
+};
+thread_local KernelTimer t_timer;
 
-// Record the caller's timing events around one GEMM launch (if set).
+void timer_release() {
+  for (cudaEvent_t e : t_timer.ev) cudaEventDestroy(e);
+  t_timer.ev.clear();
+  t_timer.used = 0;
+  t_timer.on = false;
+}
+
+// Launch one GEMM kernel, bracketed by the next event pair when timing is on.
 template <typename F>
 cudaError_t timed_launch(cudaStream_t st, F&& launch) {
-  const bool timed = t_ev_start != nullptr && t_ev_stop != nullptr;
-  if (timed) {
-    cudaError_t e = cudaEventRecord(t_ev_start, st);
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (t_timer.on && 2 * (t_timer.used + 1) <= static_cast<int64_t>(t_timer.ev.size())) {
+    e0 = t_timer.ev[2 * t_timer.used];
+    e1 = t_timer.ev[2 * t_timer.used + 1];
+  }
+  if (e0) {
+    cudaError_t e = cudaEventRecord(e0, st);
     if (e != cudaSuccess) return e;
   }
   cudaError_t e = launch();
   if (e != cudaSuccess) return e;
-  if (timed) return cudaEventRecord(t_ev_stop, st);
+  if (e1) {
+    e = cudaEventRecord(e1, st);
+    if (e != cudaSuccess) return e;
+    ++t_timer.used;
+  }
   return cudaSuccess;
 }
 
@@ -381,10 +402,42 @@ cider_status_t cider_w4a8_accumulators(const int8_t* qa, int64_t M, int64_t N, i
   return acc_entry(qa, M, N, K, qw_packed, true, group_size, acc, stream);
 }
 
-cider_status_t cider_set_gemm_events(void* ev_start, void* ev_stop) {
-  t_ev_start = static_cast<cudaEvent_t>(ev_start);
-  t_ev_stop = static_cast<cudaEvent_t>(ev_stop);
-  return CIDER_OK;
+cider_status_t cider_timing_begin(int64_t capacity) {
+  return guarded([&]() -> cider_status_t {
+    if (capacity < 1) return CIDER_ERR_INVALID_ARGUMENT;
+    timer_release();
+    t_timer.ev.resize(static_cast<size_t>(2 * capacity), nullptr);
+    for (auto& e : t_timer.ev) {
+      if (cudaEventCreate(&e) != cudaSuccess) {
+        e = nullptr;
+        timer_release();
+        return cuda_status(cudaErrorUnknown);
+      }
+    }
+    t_timer.on = true;
+    return CIDER_OK;
+  });
+}
+
+cider_status_t cider_timing_end(int64_t* count, double* total_ms) {
+  return guarded([&]() -> cider_status_t {
+    if (!count || !total_ms) return CIDER_ERR_INVALID_ARGUMENT;
+    double sum = 0.0;
+    cider_status_t st = CIDER_OK;
+    for (int64_t i = 0; i < t_timer.used; ++i) {
+      float ms = 0.0f;
+      if (cudaEventSynchronize(t_timer.ev[2 * i + 1]) != cudaSuccess ||
+          cudaEventElapsedTime(&ms, t_timer.ev[2 * i], t_timer.ev[2 * i + 1]) != cudaSuccess) {
+        st = cuda_status(cudaErrorUnknown);
+        break;
+      }
+      sum += ms;
+    }
+    *count = t_timer.used;
+    *total_ms = sum;
+    timer_release();
+    return st;
+  });
 }
 
 cider_status_t cider_check_device_error(void* stream) {
