@@ -160,6 +160,33 @@ cider_status_t cider_w4a8_accumulators(const int8_t* qa, int64_t M, int64_t N,
                                        int group_size, int32_t* acc,
                                        void* stream);
 
+/* Size of the fixed scratch array used by cider_w8a8_linear_noalloc: 32 MiB
+ * of device global memory per GPU on which the library has been used. */
+#define CIDER_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* W8A8 linear that allocates no memory.  The paper has no counterpart: this
+ * entry exists for callers that must not allocate device memory while they
+ * run, for example an inference engine that reserved almost all of HBM for
+ * weights and KV cache before serving, or a decode loop that cannot let a
+ * memory pool grow (growth can fail under memory pressure or wait on the
+ * driver).  Arguments, results and checks are those of cider_w8a8_linear;
+ * the scratch it needs (activation codes and per-token scales: M*K + 4*M
+ * bytes, rounded up to 256-byte blocks, for M <= 16, else 2*M*K + 4*M) comes
+ * from one fixed array of CIDER_NOALLOC_SCRATCH_BYTES in device memory
+ * instead of a pool; a problem that needs more returns
+ * CIDER_ERR_INVALID_ARGUMENT (for K = 2560: M above 6548).
+ *   - No cudaMalloc, cudaFree or other allocating call is made.
+ *   - The first call on each device looks up the array's device address (a
+ *     runtime call); make that first call before any stream capture.
+ *   - All calls share the one array and each call overwrites what it uses.
+ *     Calls whose kernels may overlap on the GPU (different streams without
+ *     ordering, or different host threads) race and give wrong results;
+ *     calls ordered on one stream are safe. */
+cider_status_t cider_w8a8_linear_noalloc(const void* x, int64_t M, int64_t N,
+                                         int64_t K, const int8_t* qw,
+                                         const float* sw, int granularity,
+                                         int group_size, void* y, void* stream);
+
 /* Kernel timing for benchmarks.  After cider_timing_begin(capacity), each of
  * the next `capacity` linear / accumulator calls made from the calling host
  * thread records a pair of CUDA events (created here, owned by the library)

@@ -1,0 +1,76 @@
+"""Tests of cider_w8a8_linear_noalloc, the W8A8 linear for callers that must
+not allocate device memory while they run (an engine that reserved almost all
+of HBM up front, or a decode loop that cannot let a memory pool grow).
+
+It uses one fixed scratch array in device memory instead of the library's
+memory pool, so its results must be the same as those of cider_w8a8_linear,
+call after call, even though every call reuses (and overwrites) that array.
+This file is collected last so that a stop-at-first-failure run has already
+run every other test before it.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from tests.parity_util import assert_fp16_close, require_gpu, to_host
+from w4a8_quantized_linear_gb300 import _build, inputs
+
+SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def noalloc_entry(lib):
+    f = lib.cider_w8a8_linear_noalloc
+    p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    f.argtypes = [p, i64, i64, i64, p, p, i32, i32, p, p]
+    f.restype = i32
+    return f
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M,N,K,gs", [
+    (200, 264, 1024, 0),      # tensor-core path, per channel
+    (300, 136, 2048, 128),    # tensor-core path, per group
+    (3, 136, 2560, 64),       # small-M path, per group
+    (4096, 10240, 2560, 0),   # the benchmark workload (needs 21 MB of the 32 MiB array)
+])
+def test_noalloc_matches_pooled_entry_on_consecutive_calls(M, N, K, gs):
+    cider = require_gpu()
+    f = noalloc_entry(cider.library())
+    dev = torch.device("cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    W = torch.from_numpy(inputs.weights(N, K, seed=N + K)).to(dev)
+    qw, sw = cider.cider_quantize_weight_int8(W, gs)
+    gran = cider.CIDER_PER_GROUP if gs else cider.CIDER_PER_CHANNEL
+    xs = [torch.from_numpy(inputs.activations(M, K, seed=40 + i)).to(dev) for i in range(2)]
+    ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for _ in range(2)]
+    # two calls in a row through the C ABI; the second reuses the same scratch
+    for x, y in zip(xs, ys):
+        st = f(x.data_ptr(), M, N, K, qw.data_ptr(), sw.data_ptr(), gran, gs, y.data_ptr(), stream)
+        assert st == 0, cider.library().cider_status_string(st)
+    torch.cuda.synchronize()
+    for x, y in zip(xs, ys):
+        want = cider.cider_w8a8_linear(x, qw, sw, gs)
+        assert_fp16_close(to_host(y), to_host(want), f"noalloc M={M} N={N} K={K} gs={gs}")
+    assert cider.cider_check_device_error() == 0
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch(monkeypatch):
+    """Host-side check, no GPU needed: the size limit is enforced before the
+    device is touched (CIDER_FORCE_UNSUPPORTED=1 stops well-formed calls at the
+    device check, so nothing is launched)."""
+    import w4a8_quantized_linear_gb300 as cider
+    _build.build()
+    f = noalloc_entry(cider.library())
+    monkeypatch.setenv("CIDER_FORCE_UNSUPPORTED", "1")
+    P = 0x10000
+    K = 2560
+    def need(M):  # activation codes (2*M*K bytes) and scales (4*M), in 256-byte blocks
+        return -(-2 * M * K // 256) * 256 + -(-4 * M // 256) * 256
+    m_max = max(M for M in range(6000, 7000) if need(M) <= SCRATCH_BYTES)
+    assert m_max == 6548
+    assert f(P, m_max + 1, 1024, K, P, P, 0, 0, P, None) == 1   # CIDER_ERR_INVALID_ARGUMENT
+    assert f(P, m_max, 1024, K, P, P, 0, 0, P, None) == 3       # passes the size check
+    assert f(P, 0, 1024, K, None, None, 0, 0, None, None) == 0  # empty problem
+    assert f(P, 16, 1024, K, P, P, 1, 0, P, None) == 1          # per group without a group size
