@@ -171,10 +171,11 @@ cider_status_t cider_w4a8_accumulators(const int8_t* qa, int64_t M, int64_t N,
  * memory pool grow (growth can fail under memory pressure or wait on the
  * driver).  Arguments, results and checks are those of cider_w8a8_linear;
  * the scratch it needs (activation codes and per-token scales: M*K + 4*M
- * bytes, rounded up to 256-byte blocks, for M <= 16, else 2*M*K + 4*M) comes
- * from one fixed array of CIDER_NOALLOC_SCRATCH_BYTES in device memory
- * instead of a pool; a problem that needs more returns
- * CIDER_ERR_INVALID_ARGUMENT (for K = 2560: M above 6548).
+ * bytes, each part rounded up to 256-byte blocks, for M <= 16; else
+ * 2*M*K + 4*M + 4*M, codes, scales and per-token code sums) comes from one
+ * fixed array of CIDER_NOALLOC_SCRATCH_BYTES in device memory instead of a
+ * pool; a problem that needs more returns CIDER_ERR_INVALID_ARGUMENT (for
+ * K = 2560: M above 6543).
  *   - No cudaMalloc, cudaFree or other allocating call is made.
  *   - The first call on each device looks up the array's device address (a
  *     runtime call); make that first call before any stream capture.

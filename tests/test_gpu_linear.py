@@ -189,3 +189,22 @@ def test_kernel_timing_facility(cider):
     assert n == 2 and ms > 0.0
     n, ms = cider.cider_timing_end()       # timing is off again
     assert n == 0 and ms == 0.0
+
+
+@pytest.mark.parametrize("bits,K", [(8, 2560), (4, 10240)])
+def test_mixed_fast_and_slow_token_tiles(cider, bits, K):
+    """The per-channel kernel decides per 256-token tile whether one fp32
+    accumulation over all of K is provably exact; tiles with extreme
+    activations take the chunked exact path.  Mix both kinds in one call."""
+    M, N = 700, 264
+    x = inputs.activations(M, K, seed=77)
+    rng = np.random.default_rng(78)
+    # rows of the second token tile: every code at +-127 (sum |q| = 127 K)
+    x[256:512] = (rng.choice([-1.0, 1.0], size=(256, K)) * 3.0).astype(np.float16)
+    qw_dev, qw_vals, sw = make_weights(N, K, 0, bits, seed=79)
+    qa, _ = oracle.quantize_act(x)
+    assert np.abs(qa[300].astype(np.int64)).sum() == 127 * K
+    acc = run_acc(cider, qa, qw_dev, 0, bits)
+    assert_bits_equal(acc, oracle.gemm_acc(qa, qw_vals, 0), f"mixed-tile acc bits={bits}")
+    y = run_linear(cider, x, qw_dev, sw, 0, bits)
+    assert_bits_equal(y, oracle.linear(x, qw_vals, sw, 0, threads=8), f"mixed-tile y bits={bits}")

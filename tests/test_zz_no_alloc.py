@@ -66,10 +66,10 @@ def test_noalloc_rejects_problems_beyond_its_scratch(monkeypatch):
     monkeypatch.setenv("CIDER_FORCE_UNSUPPORTED", "1")
     P = 0x10000
     K = 2560
-    def need(M):  # activation codes (2*M*K bytes) and scales (4*M), in 256-byte blocks
-        return -(-2 * M * K // 256) * 256 + -(-4 * M // 256) * 256
+    def need(M):  # codes (2*M*K bytes), scales and code sums (4*M each), in 256-byte blocks
+        return -(-2 * M * K // 256) * 256 + 2 * (-(-4 * M // 256) * 256)
     m_max = max(M for M in range(6000, 7000) if need(M) <= SCRATCH_BYTES)
-    assert m_max == 6548
+    assert m_max == 6543
     assert f(P, m_max + 1, 1024, K, P, P, 0, 0, P, None) == 1   # CIDER_ERR_INVALID_ARGUMENT
     assert f(P, m_max, 1024, K, P, P, 0, 0, P, None) == 3       # passes the size check
     assert f(P, 0, 1024, K, None, None, 0, 0, None, None) == 0  # empty problem

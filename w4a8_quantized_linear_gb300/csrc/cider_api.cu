@@ -228,23 +228,27 @@ cider_status_t run_linear(const LinearArgs& a) {
                                 a.st);
     }));
   }
-  // tensor-core path: activation codes as fp16 integers
+  // tensor-core path: activation codes as fp16 integers, scales, row sums of |code|
   const size_t qbytes = round_up(static_cast<size_t>(a.M * a.K) * 2, 256);
-  cudaError_t e = scratch_alloc(scratch, dev, qbytes + round_up(4 * a.M, 256), a.st);
+  const size_t vbytes = round_up(4 * a.M, 256);
+  cudaError_t e = scratch_alloc(scratch, dev, qbytes + 2 * vbytes, a.st);
   if (e != cudaSuccess) return cuda_status(e);
-  __half* q16 = static_cast<__half*>(scratch.ptr);
+  uint8_t* sbase = static_cast<uint8_t*>(scratch.ptr);
+  __half* q16 = reinterpret_cast<__half*>(sbase);
+  int* row_l1 = reinterpret_cast<int*>(sbase + qbytes + vbytes);
   const float* sa = a.sa;
   if (a.x) {
-    float* sscr = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch.ptr) + qbytes);
-    e = cider::launch_quant_act_f16(static_cast<const __half*>(a.x), a.M, a.K, q16, sscr, a.st);
+    float* sscr = reinterpret_cast<float*>(sbase + qbytes);
+    e = cider::launch_quant_act_f16(static_cast<const __half*>(a.x), a.M, a.K, q16, sscr, row_l1,
+                                    a.st);
     sa = sscr;
   } else {
-    e = cider::launch_codes_s8_to_f16(a.qa, a.M * a.K, q16, a.st);
+    e = cider::launch_codes_s8_to_f16(a.qa, a.M, a.K, q16, row_l1, a.st);
   }
   if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(timed_launch(a.st, [&] {
-    return cider::launch_gemm_tc(q16, sa, a.M, a.N, a.K, w, a.int4, a.sw, gs, a.mode, y, a.acc,
-                                 sms, a.st);
+    return cider::launch_gemm_tc(q16, sa, row_l1, a.M, a.N, a.K, w, a.int4, a.sw, gs, a.mode, y,
+                                 a.acc, sms, a.st);
   }));
 }
 

@@ -33,11 +33,13 @@ enum EpiMode : int {
 // quant.cu
 cudaError_t launch_quant_act_s8(const __half* x, int64_t M, int64_t K, int8_t* q, float* sa,
                                 cudaStream_t st);
+// fp16 codes for the tensor-core path, plus row_l1[m] = sum_k |q[m,k]|.
 cudaError_t launch_quant_act_f16(const __half* x, int64_t M, int64_t K, __half* q, float* sa,
-                                 cudaStream_t st);
+                                 int* row_l1, cudaStream_t st);
 cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int group_size, bool int4,
                                 uint8_t* q, float* sw, cudaStream_t st);
-cudaError_t launch_codes_s8_to_f16(const int8_t* qa, int64_t count, __half* out, cudaStream_t st);
+cudaError_t launch_codes_s8_to_f16(const int8_t* qa, int64_t M, int64_t K, __half* out,
+                                   int* row_l1, cudaStream_t st);
 
 // gemv.cu: small-M weight-streaming path.  qa int8 [M, K] (M <= 16).
 // group_size 0 = per channel.  Exactly one of y / acc is used (by mode).
@@ -47,10 +49,12 @@ cudaError_t launch_gemv(const int8_t* qa, const float* sa, int64_t M, int64_t N,
                         __half* y, int32_t* acc, int num_sms, cudaStream_t st);
 
 // gemm_tc.cu: tensor-core path.  qa16 holds the activation codes as fp16
-// integers [M, K].
-cudaError_t launch_gemm_tc(const __half* qa16, const float* sa, int64_t M, int64_t N, int64_t K,
-                           const uint8_t* w, bool int4, const float* sw, int group_size,
-                           int mode, __half* y, int32_t* acc, int num_sms, cudaStream_t st);
+// integers [M, K]; row_l1[m] = sum_k |code| (used by the per-channel kernel
+// to decide per tile whether one fp32 accumulation over all of K is exact).
+cudaError_t launch_gemm_tc(const __half* qa16, const float* sa, const int* row_l1, int64_t M,
+                           int64_t N, int64_t K, const uint8_t* w, bool int4, const float* sw,
+                           int group_size, int mode, __half* y, int32_t* acc, int num_sms,
+                           cudaStream_t st);
 cudaError_t read_and_clear_device_error(int* value);
 cudaError_t launch_debug_wait_timeout(int64_t max_polls, cudaStream_t st);
 

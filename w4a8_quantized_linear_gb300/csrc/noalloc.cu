@@ -72,12 +72,13 @@ cider_status_t scratch_for_current_device(void** out, int* num_sms) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Scratch bytes one call needs: activation codes plus per-token scales.
+// Scratch bytes one call needs: activation codes, per-token scales and (for
+// the tensor-core path) per-token sums of |code|.
 size_t noalloc_scratch_bytes(int64_t M, int64_t K) {
   if (M <= 0 || K <= 0) return 0;
   const size_t mk = static_cast<size_t>(M) * static_cast<size_t>(K);
   if (cider::gemv_fits(M, K)) return round256(mk) + round256(4 * static_cast<size_t>(M));
-  return round256(2 * mk) + round256(4 * static_cast<size_t>(M));
+  return round256(2 * mk) + 2 * round256(4 * static_cast<size_t>(M));
 }
 
 }  // namespace
@@ -124,12 +125,14 @@ extern "C" cider_status_t cider_w8a8_linear_noalloc(const void* x, int64_t M, in
                                sms, st);
     } else {
       const size_t qbytes = round256(2 * static_cast<size_t>(M) * static_cast<size_t>(K));
+      const size_t vbytes = round256(4 * static_cast<size_t>(M));
       __half* q16 = reinterpret_cast<__half*>(base);
       float* sa = reinterpret_cast<float*>(base + qbytes);
-      e = cider::launch_quant_act_f16(static_cast<const __half*>(x), M, K, q16, sa, st);
+      int* row_l1 = reinterpret_cast<int*>(base + qbytes + vbytes);
+      e = cider::launch_quant_act_f16(static_cast<const __half*>(x), M, K, q16, sa, row_l1, st);
       if (e == cudaSuccess)
-        e = cider::launch_gemm_tc(q16, sa, M, N, K, w, false, sw, group_size, cider::kEpiY, yh,
-                                  nullptr, sms, st);
+        e = cider::launch_gemm_tc(q16, sa, row_l1, M, N, K, w, false, sw, group_size, cider::kEpiY,
+                                  yh, nullptr, sms, st);
     }
     if (e != cudaSuccess) {
       cudaGetLastError();

@@ -41,9 +41,10 @@ __device__ __forceinline__ float quant_code(float x, float s) {
 
 // Eight fp16 values -> eight codes, stored as int8 (8 bytes) or as fp16
 // integers (16 bytes; exact, the operand format of the tensor-core GEMM).
-__device__ __forceinline__ void store_codes(int8_t* q, int64_t off, const uint4& v, float s) {
+__device__ __forceinline__ int store_codes(int8_t* q, int64_t off, const uint4& v, float s) {
   const __half2* h = reinterpret_cast<const __half2*>(&v);
   uint32_t w[2];
+  int l1 = 0;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     uint32_t b = 0;
@@ -52,24 +53,39 @@ __device__ __forceinline__ void store_codes(int8_t* q, int64_t off, const uint4&
       float2 f = __half22float2(h[2 * j + e]);
       int c0 = static_cast<int>(quant_code(f.x, s));
       int c1 = static_cast<int>(quant_code(f.y, s));
+      l1 += abs(c0) + abs(c1);
       b |= (static_cast<uint32_t>(c0 & 0xFF) << (16 * e)) |
            (static_cast<uint32_t>(c1 & 0xFF) << (16 * e + 8));
     }
     w[j] = b;
   }
   *reinterpret_cast<uint2*>(q + off) = make_uint2(w[0], w[1]);
+  return l1;
 }
-__device__ __forceinline__ void store_codes(__half* q, int64_t off, const uint4& v, float s) {
+__device__ __forceinline__ int store_codes(__half* q, int64_t off, const uint4& v, float s) {
   const __half2* h = reinterpret_cast<const __half2*>(&v);
   uint4 o;
   uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+  float l1 = 0.0f;  // a sum of at most 8 codes: exact
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     float2 f = __half22float2(h[j]);
-    __half2 r = __floats2half2_rn(quant_code(f.x, s), quant_code(f.y, s));
+    const float c0 = quant_code(f.x, s), c1 = quant_code(f.y, s);
+    l1 += fabsf(c0) + fabsf(c1);
+    __half2 r = __floats2half2_rn(c0, c1);
     ow[j] = *reinterpret_cast<uint32_t*>(&r);
   }
   *reinterpret_cast<uint4*>(q + off) = o;
+  return static_cast<int>(l1);
+}
+
+__device__ __forceinline__ int block_sum_128(int v, int* red) {
+  v = __reduce_add_sync(0xffffffffu, v);
+  __syncthreads();  // red may still be read by a previous reduction
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[warp] = v;
+  __syncthreads();
+  return red[0] + red[1] + red[2] + red[3];
 }
 
 // One CTA of 128 threads per row; the row stays in registers between the
@@ -77,8 +93,10 @@ __device__ __forceinline__ void store_codes(__half* q, int64_t off, const uint4&
 template <typename OutT, int VPT>
 __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const __half* __restrict__ x,
                                                                   int64_t K, OutT* __restrict__ q,
-                                                                  float* __restrict__ sa) {
+                                                                  float* __restrict__ sa,
+                                                                  int* __restrict__ row_l1) {
   __shared__ float red[4];
+  __shared__ int ired[4];
   const int64_t m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(x + m * K);
   const int nvec = static_cast<int>(K >> 3);
@@ -98,10 +116,15 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const __half* 
   amax = block_max_128(amax, red);
   const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
   if (threadIdx.x == 0) sa[m] = s;
+  int l1 = 0;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int idx = threadIdx.x + i * kQuantThreads;
-    if (idx < nvec) store_codes(q, m * K + static_cast<int64_t>(idx) * 8, v[i], s);
+    if (idx < nvec) l1 += store_codes(q, m * K + static_cast<int64_t>(idx) * 8, v[i], s);
+  }
+  if (row_l1 != nullptr) {
+    l1 = block_sum_128(l1, ired);
+    if (threadIdx.x == 0) row_l1[m] = l1;
   }
 }
 
@@ -111,8 +134,10 @@ template <typename OutT>
 __global__ void __launch_bounds__(kQuantThreads) quant_act_long_kernel(const __half* __restrict__ x,
                                                                        int64_t K,
                                                                        OutT* __restrict__ q,
-                                                                       float* __restrict__ sa) {
+                                                                       float* __restrict__ sa,
+                                                                       int* __restrict__ row_l1) {
   __shared__ float red[4];
+  __shared__ int ired[4];
   const int64_t m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(x + m * K);
   const int64_t nvec = K >> 3;
@@ -127,34 +152,39 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_long_kernel(const __h
   amax = block_max_128(amax, red);
   const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
   if (threadIdx.x == 0) sa[m] = s;
+  int l1 = 0;
   for (int64_t idx = threadIdx.x; idx < nvec; idx += kQuantThreads)
-    store_codes(q, m * K + idx * 8, row[idx], s);
+    l1 += store_codes(q, m * K + idx * 8, row[idx], s);
+  if (row_l1 != nullptr) {
+    l1 = block_sum_128(l1, ired);
+    if (threadIdx.x == 0) row_l1[m] = l1;
+  }
 }
 
 template <typename OutT>
 cudaError_t launch_quant_act(const __half* x, int64_t M, int64_t K, OutT* q, float* sa,
-                             cudaStream_t st) {
+                             int* row_l1, cudaStream_t st) {
   const int64_t nvec = K / 8;
   const int vpt = static_cast<int>((nvec + kQuantThreads - 1) / kQuantThreads);
   const dim3 grid(static_cast<unsigned>(M));
   if (vpt <= 1)
-    quant_act_kernel<OutT, 1><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+    quant_act_kernel<OutT, 1><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
   else if (vpt <= 2)
-    quant_act_kernel<OutT, 2><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+    quant_act_kernel<OutT, 2><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
   else if (vpt <= 3)
-    quant_act_kernel<OutT, 3><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+    quant_act_kernel<OutT, 3><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
   else if (vpt <= 4)
-    quant_act_kernel<OutT, 4><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+    quant_act_kernel<OutT, 4><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
   else if (vpt <= 6)
-    quant_act_kernel<OutT, 6><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+    quant_act_kernel<OutT, 6><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
   else if (vpt <= 8)
-    quant_act_kernel<OutT, 8><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+    quant_act_kernel<OutT, 8><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
   else if (vpt <= 12)
-    quant_act_kernel<OutT, 12><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+    quant_act_kernel<OutT, 12><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
   else if (vpt <= 16)
-    quant_act_kernel<OutT, 16><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+    quant_act_kernel<OutT, 16><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
   else
-    quant_act_long_kernel<OutT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa);
+    quant_act_long_kernel<OutT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
   return cudaGetLastError();
 }
 
@@ -199,33 +229,48 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const float* __restri
   }
 }
 
-// int8 codes -> the same codes as fp16 integers (exact), 16 per thread.
-__global__ void __launch_bounds__(256) codes_s8_to_f16_kernel(const int8_t* __restrict__ qa,
-                                                              int64_t n16,
-                                                              __half* __restrict__ out) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n16) return;
-  const uint4 v = ld_stream_v4(qa + i * 16);
-  uint4 o0, o1;
-  s8x4_to_h2x2(v.x, o0.x, o0.y);
-  s8x4_to_h2x2(v.y, o0.z, o0.w);
-  s8x4_to_h2x2(v.z, o1.x, o1.y);
-  s8x4_to_h2x2(v.w, o1.z, o1.w);
-  uint4* dst = reinterpret_cast<uint4*>(out + i * 16);
-  dst[0] = o0;
-  dst[1] = o1;
+// int8 codes -> the same codes as fp16 integers (exact), one CTA per row,
+// plus the row's sum of |code|.
+__global__ void __launch_bounds__(kQuantThreads) codes_s8_to_f16_kernel(const int8_t* __restrict__ qa,
+                                                                        int64_t K,
+                                                                        __half* __restrict__ out,
+                                                                        int* __restrict__ row_l1) {
+  __shared__ int ired[4];
+  const int64_t m = blockIdx.x;
+  const int64_t n16 = K / 16;
+  int l1 = 0;
+  for (int64_t i = threadIdx.x; i < n16; i += kQuantThreads) {
+    const uint4 v = ld_stream_v4(qa + m * K + i * 16);
+    const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int b0 = static_cast<int8_t>(vw[j] & 0xFF), b1 = static_cast<int8_t>((vw[j] >> 8) & 0xFF);
+      const int b2 = static_cast<int8_t>((vw[j] >> 16) & 0xFF), b3 = static_cast<int8_t>(vw[j] >> 24);
+      l1 += abs(b0) + abs(b1) + abs(b2) + abs(b3);
+    }
+    uint4 o0, o1;
+    s8x4_to_h2x2(v.x, o0.x, o0.y);
+    s8x4_to_h2x2(v.y, o0.z, o0.w);
+    s8x4_to_h2x2(v.z, o1.x, o1.y);
+    s8x4_to_h2x2(v.w, o1.z, o1.w);
+    uint4* dst = reinterpret_cast<uint4*>(out + m * K + i * 16);
+    dst[0] = o0;
+    dst[1] = o1;
+  }
+  l1 = block_sum_128(l1, ired);
+  if (threadIdx.x == 0) row_l1[m] = l1;
 }
 
 }  // namespace
 
 cudaError_t launch_quant_act_s8(const __half* x, int64_t M, int64_t K, int8_t* q, float* sa,
                                 cudaStream_t st) {
-  return launch_quant_act<int8_t>(x, M, K, q, sa, st);
+  return launch_quant_act<int8_t>(x, M, K, q, sa, nullptr, st);
 }
 
 cudaError_t launch_quant_act_f16(const __half* x, int64_t M, int64_t K, __half* q, float* sa,
-                                 cudaStream_t st) {
-  return launch_quant_act<__half>(x, M, K, q, sa, st);
+                                 int* row_l1, cudaStream_t st) {
+  return launch_quant_act<__half>(x, M, K, q, sa, row_l1, st);
 }
 
 cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int group_size, bool int4,
@@ -240,10 +285,9 @@ cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int group_
   return cudaGetLastError();
 }
 
-cudaError_t launch_codes_s8_to_f16(const int8_t* qa, int64_t count, __half* out, cudaStream_t st) {
-  const int64_t n16 = count / 16;
-  const int64_t blocks = (n16 + 255) / 256;
-  codes_s8_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(qa, n16, out);
+cudaError_t launch_codes_s8_to_f16(const int8_t* qa, int64_t M, int64_t K, __half* out,
+                                   int* row_l1, cudaStream_t st) {
+  codes_s8_to_f16_kernel<<<static_cast<unsigned>(M), kQuantThreads, 0, st>>>(qa, K, out, row_l1);
   return cudaGetLastError();
 }
 
