@@ -63,6 +63,9 @@ def parse_args():
     ap.add_argument("--bits", type=int, default=8, choices=[8, 4])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
+                    help="replay the timed steps from a CUDA graph (auto: for M <= 16, where "
+                         "one layer call is shorter than its host-side launch path)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -296,7 +299,23 @@ def run_ours(a):
         step(i)
     torch.cuda.synchronize()
 
-    cider.cider_timing_begin(a.steps)   # events are created here, outside the timed region
+    use_graph = a.graph == "on" or (a.graph == "auto" and a.M <= 16)
+    graph = None
+    per_graph = 1
+    if use_graph:
+        # one graph holds `per_graph` consecutive steps (a divisor of K), replayed K / per_graph times
+        per_graph = max(d for d in range(1, min(a.steps, 64) + 1) if a.steps % d == 0)
+        cider.cider_timing_begin(per_graph)    # the kernel-timing events become graph nodes
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(per_graph):
+                step(i)
+        torch.cuda.synchronize()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+    else:
+        cider.cider_timing_begin(a.steps)   # events are created here, outside the timed region
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local) if rank == 0 else None
     if clocks:
@@ -308,8 +327,12 @@ def run_ours(a):
     if clocks:
         clocks.mark(True)
     start.record()
-    for i in range(a.steps):
-        step(i)
+    if graph is not None:
+        for _ in range(a.steps // per_graph):
+            graph.replay()
+    else:
+        for i in range(a.steps):
+            step(i)
     stop.record()
     torch.cuda.synchronize()
     if clocks:
@@ -319,7 +342,8 @@ def run_ours(a):
         torch.distributed.barrier()
     clk = clocks.stop() if clocks else None
     el_ms = start.elapsed_time(stop)
-    assert n_timed == a.steps, (n_timed, a.steps)
+    # with a graph, the events hold the last replay's `per_graph` launches
+    assert n_timed == (per_graph if graph is not None else a.steps), (n_timed, a.steps)
     if cider.cider_check_device_error() != 0:
         raise SystemExit("libcider reported a timed-out wait inside a kernel")
     if ws > 1:
@@ -401,7 +425,9 @@ def run_ours(a):
                    "bits": a.bits, "parallelism": f"replicas x{ws}",
                    "l2": f"inputs larger than L2: {n_sets} rotating x/qw/y sets "
                          f"({n_sets * set_bytes / 1e6:.0f} MB)",
-                   "gemm_ms_avg": gemm_avg_s * 1e3},
+                   "gemm_ms_avg": gemm_avg_s * 1e3,
+                   "launch": (f"CUDA graph of {per_graph} steps, replayed {a.steps // per_graph} times"
+                              if graph is not None else "direct launches from Python")},
         "roofline": roof,
         "gpu_launches": 2 * a.steps,
         "e2e": e2e,

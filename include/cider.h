@@ -110,7 +110,8 @@ cider_status_t cider_quantize_weight_int4(const float* w, int64_t N, int64_t K,
  * matmul_fused_dequant).  Quantizes x per token on the device (scratch from
  * the library's stream-ordered pool), then runs the integer GEMM with the
  * dequant fused into its store.  M <= 16 uses the weight-streaming GEMV path,
- * larger M the tensor-core GEMM.
+ * larger M the tensor-core GEMM (the small-M kernel quantizes the rows
+ * itself and needs no scratch).
  *   x     fp16 [M, K]
  *   qw    int8 [N, K]       (out_features x in_features, nn.Linear layout)
  *   sw    fp32 [N] (granularity CIDER_PER_CHANNEL, group_size 0)
@@ -170,12 +171,12 @@ cider_status_t cider_w4a8_accumulators(const int8_t* qa, int64_t M, int64_t N,
  * weights and KV cache before serving, or a decode loop that cannot let a
  * memory pool grow (growth can fail under memory pressure or wait on the
  * driver).  Arguments, results and checks are those of cider_w8a8_linear;
- * the scratch it needs (activation codes and per-token scales: M*K + 4*M
- * bytes, each part rounded up to 256-byte blocks, for M <= 16; else
- * 2*M*K + 4*M + 4*M, codes, scales and per-token code sums) comes from one
- * fixed array of CIDER_NOALLOC_SCRATCH_BYTES in device memory instead of a
- * pool; a problem that needs more returns CIDER_ERR_INVALID_ARGUMENT (for
- * K = 2560: M above 6543).
+ * the scratch it needs (none for M <= 16; else activation codes, per-token
+ * scales and per-token code sums, 2*M*K + 4*M + 4*M bytes, each part
+ * rounded up to 256-byte blocks) comes from one fixed array of
+ * CIDER_NOALLOC_SCRATCH_BYTES in device memory instead of a pool; a problem
+ * that needs more returns CIDER_ERR_INVALID_ARGUMENT (for K = 2560: M above
+ * 6543).
  *   - No cudaMalloc, cudaFree or other allocating call is made.
  *   - The first call on each device looks up the array's device address (a
  *     runtime call); make that first call before any stream capture.
@@ -192,7 +193,8 @@ cider_status_t cider_w8a8_linear_noalloc(const void* x, int64_t M, int64_t N,
  * the next `capacity` linear / accumulator calls made from the calling host
  * thread records a pair of CUDA events (created here, owned by the library)
  * on its stream immediately before and after launching its integer-GEMM
- * kernel (the tensor-core GEMM, or the GEMV for M <= 16).
+ * kernel (the tensor-core GEMM, or the GEMV for M <= 16); during a stream
+ * capture the records become graph nodes and time the kernel at each replay.
  * cider_timing_end waits for those events, writes the number of timed
  * launches and their summed device time in milliseconds, releases the events
  * and stops timing.  Returns CIDER_ERR_CUDA if an event call fails,

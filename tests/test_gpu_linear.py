@@ -48,7 +48,7 @@ def run_linear(cider, x, qw_dev_arr, sw, gs, bits):
 SHAPES = [  # (M, N, K): GEMV bucket (M <= 16) and GEMM tiles with ragged edges
     (1, 8, 128), (1, 136, 2560), (3, 64, 544), (5, 256, 1024), (16, 200, 2048),
     (17, 136, 128), (64, 256, 576), (128, 128, 2560), (130, 264, 1088), (300, 200, 2048),
-    (257, 384, 4096),
+    (257, 384, 4096), (300, 136, 4608), (40, 264, 6144),
 ]
 
 
@@ -68,9 +68,9 @@ def test_accumulators_bit_exact(cider, M, N, K, gs, bits):
 @pytest.mark.parametrize("bits", [8, 4])
 @pytest.mark.parametrize("M", [4, 160])
 def test_accumulators_exact_beyond_fp32_significand(cider, M, bits):
-    """All codes at the extreme: |acc| = 16129 K (8-bit) reaches 4.1e7 > 2^24
-    at K = 2560; plus rows mixing large products with +-1 products."""
-    N, K = 136, 2560
+    """All codes at the extreme: |acc| = 16129 K (8-bit) reaches 8.3e7 > 2^24
+    at K = 5120; plus rows mixing large products with +-1 products."""
+    N, K = 136, (2560 if M == 4 else 5120)
     qa = np.full((M, K), 127, np.int8)
     qa[1::2] = -127
     qa[2, :] = 1
@@ -191,7 +191,7 @@ def test_kernel_timing_facility(cider):
     assert n == 0 and ms == 0.0
 
 
-@pytest.mark.parametrize("bits,K", [(8, 2560), (4, 10240)])
+@pytest.mark.parametrize("bits,K", [(8, 2560), (4, 10240), (8, 6144)])
 def test_mixed_fast_and_slow_token_tiles(cider, bits, K):
     """The per-channel kernel decides per 256-token tile whether one fp32
     accumulation over all of K is provably exact; tiles with extreme
@@ -208,3 +208,43 @@ def test_mixed_fast_and_slow_token_tiles(cider, bits, K):
     assert_bits_equal(acc, oracle.gemm_acc(qa, qw_vals, 0), f"mixed-tile acc bits={bits}")
     y = run_linear(cider, x, qw_dev, sw, 0, bits)
     assert_bits_equal(y, oracle.linear(x, qw_vals, sw, 0, threads=8), f"mixed-tile y bits={bits}")
+
+
+@pytest.mark.parametrize("M,N,K,gs,bits", [(1, 264, 1024, 0, 8), (16, 136, 2048, 128, 4),
+                                           (300, 264, 1024, 0, 8), (200, 136, 1024, 64, 8)])
+def test_linear_replays_from_cuda_graph(cider, M, N, K, gs, bits):
+    """The entry points enqueue only stream-ordered work (kernels, pool
+    allocations), so a captured call replays to the same bits as an eager one."""
+    x = to_dev(inputs.activations(M, K, seed=90))
+    qw_dev, _, sw = make_weights(N, K, gs, bits, seed=91)
+    qw_d, sw_d = to_dev(qw_dev), to_dev(sw)
+    lin = cider.cider_w8a8_linear if bits == 8 else cider.cider_w4a8_linear
+    want = lin(x, qw_d, sw_d, gs)
+    y = torch.zeros_like(want)
+    lin(x, qw_d, sw_d, gs, out=y)              # warm-up outside capture
+    torch.cuda.synchronize()
+    y.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        lin(x, qw_d, sw_d, gs, out=y)
+    for _ in range(2):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert_bits_equal(to_host(y), to_host(want), "graph replay")
+
+
+def test_kernel_timing_inside_cuda_graph(cider):
+    M, N, K = 1, 1024, 2048
+    x = torch.from_numpy(inputs.activations(M, K, seed=3)).cuda()
+    qw, sw = cider.cider_quantize_weight_int8(torch.from_numpy(inputs.weights(N, K)).cuda(), 0)
+    y = cider.cider_w8a8_linear(x, qw, sw, 0)
+    torch.cuda.synchronize()
+    cider.cider_timing_begin(2)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cider.cider_w8a8_linear(x, qw, sw, 0, out=y)
+        cider.cider_w8a8_linear(x, qw, sw, 0, out=y)
+    g.replay()
+    n, ms = cider.cider_timing_end()
+    assert n == 2 and 0.0 < ms < 100.0

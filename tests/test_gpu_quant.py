@@ -73,3 +73,29 @@ def test_quantize_weight_int4_bit_exact(cider, N, K, gs):
 
 def test_no_device_error_left(cider):
     assert cider.cider_check_device_error() == 0
+
+
+def _exhaustive_amax_values():
+    rng = np.random.default_rng(2024)
+    fixed = [65504.0, 1.0, 127.0, 3.140625, 0.0009765625, 2.0 ** -24 * 37, 2.0 ** -14, 1000.0,
+             0.0016956329345703125, 0.50732421875, 2.0 ** -24, 6.0e-5, 0.3333, 254.0, 8191.0]
+    allv = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16).view(np.float16)
+    pos = allv[np.isfinite(allv) & (allv > 0)]
+    return fixed + [float(v) for v in rng.choice(pos, 25, replace=False)]
+
+
+@pytest.mark.parametrize("amax", _exhaustive_amax_values())
+def test_quantize_act_exhaustive_fp16_values(cider, amax):
+    """Every finite fp16 value |x| <= amax, in rows whose maximum is amax: codes
+    and scales bit-exact against the oracle (exercises the division, rounding
+    and clamp for all inputs a scale can see)."""
+    allv = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16).view(np.float16)
+    vals = allv[np.isfinite(allv) & (np.abs(allv.astype(np.float64)) <= amax)]
+    W = 2048
+    pad = (-len(vals)) % (W - 1)
+    vals = np.concatenate([vals, np.zeros(pad, np.float16)]).reshape(-1, W - 1)
+    x = np.concatenate([np.full((vals.shape[0], 1), amax, np.float16), vals], axis=1)
+    qa, sa = cider.cider_quantize_act(to_dev(x))
+    qref, sref = oracle.quantize_act(x)
+    assert_bits_equal(to_host(sa).view(np.uint32), sref.view(np.uint32), "s_a")
+    assert_bits_equal(to_host(qa), qref, "q_a")

@@ -137,6 +137,16 @@ void timer_release() {
   t_timer.on = false;
 }
 
+// Record a timing event; inside a stream capture the record must become a
+// graph node (an external record), or it would only mark a dependency.
+cudaError_t record_timing_event(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+  return cudaEventRecord(ev, st);
+}
+
 // Launch one GEMM kernel, bracketed by the next event pair when timing is on.
 template <typename F>
 cudaError_t timed_launch(cudaStream_t st, F&& launch) {
@@ -146,13 +156,13 @@ cudaError_t timed_launch(cudaStream_t st, F&& launch) {
     e1 = t_timer.ev[2 * t_timer.used + 1];
   }
   if (e0) {
-    cudaError_t e = cudaEventRecord(e0, st);
+    cudaError_t e = record_timing_event(e0, st);
     if (e != cudaSuccess) return e;
   }
   cudaError_t e = launch();
   if (e != cudaSuccess) return e;
   if (e1) {
-    e = cudaEventRecord(e1, st);
+    e = record_timing_event(e1, st);
     if (e != cudaSuccess) return e;
     ++t_timer.used;
   }
@@ -210,22 +220,10 @@ cider_status_t run_linear(const LinearArgs& a) {
   const int gs = a.group_size;
   Scratch scratch;
   if (cider::gemv_fits(a.M, a.K)) {
-    const int8_t* qa = a.qa;
-    const float* sa = a.sa;
-    if (a.x) {
-      const size_t qbytes = round_up(static_cast<size_t>(a.M * a.K), 256);
-      cudaError_t e = scratch_alloc(scratch, dev, qbytes + round_up(4 * a.M, 256), a.st);
-      if (e != cudaSuccess) return cuda_status(e);
-      int8_t* q = static_cast<int8_t*>(scratch.ptr);
-      float* sscr = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch.ptr) + qbytes);
-      e = cider::launch_quant_act_s8(static_cast<const __half*>(a.x), a.M, a.K, q, sscr, a.st);
-      if (e != cudaSuccess) return cuda_status(e);
-      qa = q;
-      sa = sscr;
-    }
+    // small M: one kernel, quantizing the activation rows itself when given x
     return cuda_status(timed_launch(a.st, [&] {
-      return cider::launch_gemv(qa, sa, a.M, a.N, a.K, w, a.int4, a.sw, gs, a.mode, y, a.acc, sms,
-                                a.st);
+      return cider::launch_gemv(static_cast<const __half*>(a.x), a.qa, a.sa, a.M, a.N, a.K, w,
+                                a.int4, a.sw, gs, a.mode, y, a.acc, sms, a.st);
     }));
   }
   // tensor-core path: activation codes as fp16 integers, scales, row sums of |code|

@@ -17,6 +17,11 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Barrier over `count` threads (a multiple of 32) of the CTA, with id 1..15.
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -49,6 +54,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// As mbar_wait_bounded, but polling with the non-blocking test_wait (the
+// thread never suspends): for short waits on data that is almost there.
+__device__ __forceinline__ bool mbar_spin_bounded(uint32_t bar, uint32_t parity,
+                                                  volatile uint32_t* abort_flag, int* err,
+                                                  uint64_t timeout_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint64_t n = 1;; ++n) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((n & 255) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > timeout_ns) {
+        *abort_flag = 1u;
+        atomicOr(err, kDevErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait for the phase with the given parity.  Gives up when another
 // thread of the CTA raised `abort_flag`, after `max_polls` polls (0 = no poll
 // limit), or after `timeout_ns` of global time; a give-up of its own sets
@@ -79,6 +116,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+// Contiguous global -> shared copy by the TMA engine, completing `bytes` of
+// transaction count on `bar`.  Addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
@@ -120,6 +167,21 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16, one CTA.
+__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (TMA, tensor core).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -220,6 +282,26 @@ __device__ __forceinline__ void s4x8_to_h2x4(uint32_t w, uint32_t (&h)[4]) {
     __half2 r = __hfma2(*reinterpret_cast<__half2*>(&x), scale, bias);
     h[j] = *reinterpret_cast<uint32_t*>(&r);
   }
+}
+
+// x / s correctly rounded (IEEE binary32, round to nearest even), from
+// r = RN(1/s) and two FMAs: q0 = RN(x r) is within one ulp of x / s, the
+// residual x - s q0 is exact in one FMA, and RN(q0 + residual * r) is the
+// correctly rounded quotient (Markstein's theorem; P. Markstein, "IA-64 and
+// Elementary Functions", 2000; J.-M. Muller et al., "Handbook of
+// Floating-Point Arithmetic", division by FMA).  The theorem needs no
+// overflow or underflow on the way, which holds here: |x / s| <= 127 and the
+// residual is at least 2^-24 |s q0| whenever it is not zero.
+__device__ __forceinline__ float div_rn_by(float x, float s, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float e = __fmaf_rn(-q0, s, x);
+  return __fmaf_rn(e, r, q0);
+}
+
+// Symmetric INT8 code of x for scale s (r = RN(1/s)): clamp(rint(x / s), +-127).
+__device__ __forceinline__ float act_code(float x, float s, float r) {
+  const float q = rintf(div_rn_by(x, s, r));
+  return fminf(fmaxf(q, -127.0f), 127.0f);
 }
 
 // Four INT4 codes in the low nibbles of the bytes of t (high nibbles zero),

@@ -6,9 +6,18 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cuda.h>
+
 #include <atomic>
 
 namespace cider {
+
+// 2D TMA tensor map over a row-major matrix: `inner` elements per row,
+// `outer` rows, `row_bytes` between rows; box of box_inner x box_outer.
+// Out-of-bounds elements of a box read as zero.  Returns false on failure.
+bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, uint64_t inner,
+                        uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                        CUtensorMapSwizzle swz);
 
 // Raise a kernel's dynamic shared memory limit once per device (bit d of
 // `done` records device d).
@@ -41,12 +50,14 @@ cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int group_
 cudaError_t launch_codes_s8_to_f16(const int8_t* qa, int64_t M, int64_t K, __half* out,
                                    int* row_l1, cudaStream_t st);
 
-// gemv.cu: small-M weight-streaming path.  qa int8 [M, K] (M <= 16).
-// group_size 0 = per channel.  Exactly one of y / acc is used (by mode).
+// gemv.cu: small-M weight-streaming path (M <= 16).  Activations either as
+// fp16 x [M, K] (quantized inside the kernel; x != nullptr) or as codes
+// qa int8 [M, K] with scales sa [M].  group_size 0 = per channel.  Exactly
+// one of y / acc is used (by mode).
 bool gemv_fits(int64_t M, int64_t K);
-cudaError_t launch_gemv(const int8_t* qa, const float* sa, int64_t M, int64_t N, int64_t K,
-                        const uint8_t* w, bool int4, const float* sw, int group_size, int mode,
-                        __half* y, int32_t* acc, int num_sms, cudaStream_t st);
+cudaError_t launch_gemv(const __half* x, const int8_t* qa, const float* sa, int64_t M, int64_t N,
+                        int64_t K, const uint8_t* w, bool int4, const float* sw, int group_size,
+                        int mode, __half* y, int32_t* acc, int num_sms, cudaStream_t st);
 
 // gemm_tc.cu: tensor-core path.  qa16 holds the activation codes as fp16
 // integers [M, K]; row_l1[m] = sum_k |code| (used by the per-channel kernel
@@ -56,6 +67,9 @@ cudaError_t launch_gemm_tc(const __half* qa16, const float* sa, const int* row_l
                            int group_size, int mode, __half* y, int32_t* acc, int num_sms,
                            cudaStream_t st);
 cudaError_t read_and_clear_device_error(int* value);
+// Device address of the library's error word on the current device.
+cudaError_t device_error_word(int** ptr);
+constexpr uint64_t kKernelWaitTimeoutNs = 2000000000ull;
 cudaError_t launch_debug_wait_timeout(int64_t max_polls, cudaStream_t st);
 
 }  // namespace cider

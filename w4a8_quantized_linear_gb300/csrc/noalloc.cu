@@ -72,12 +72,12 @@ cider_status_t scratch_for_current_device(void** out, int* num_sms) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Scratch bytes one call needs: activation codes, per-token scales and (for
-// the tensor-core path) per-token sums of |code|.
+// Scratch bytes one call needs: for the tensor-core path the activation
+// codes, per-token scales and per-token sums of |code|; none for small M.
 size_t noalloc_scratch_bytes(int64_t M, int64_t K) {
   if (M <= 0 || K <= 0) return 0;
   const size_t mk = static_cast<size_t>(M) * static_cast<size_t>(K);
-  if (cider::gemv_fits(M, K)) return round256(mk) + round256(4 * static_cast<size_t>(M));
+  if (cider::gemv_fits(M, K)) return 0;  // the small-M kernel quantizes in shared memory
   return round256(2 * mk) + 2 * round256(4 * static_cast<size_t>(M));
 }
 
@@ -115,14 +115,10 @@ extern "C" cider_status_t cider_w8a8_linear_noalloc(const void* x, int64_t M, in
     __half* yh = static_cast<__half*>(y);
     uint8_t* base = static_cast<uint8_t*>(scratch);
     cudaError_t e;
+    (void)base;
     if (cider::gemv_fits(M, K)) {
-      const size_t qbytes = round256(static_cast<size_t>(M) * static_cast<size_t>(K));
-      int8_t* q = reinterpret_cast<int8_t*>(base);
-      float* sa = reinterpret_cast<float*>(base + qbytes);
-      e = cider::launch_quant_act_s8(static_cast<const __half*>(x), M, K, q, sa, st);
-      if (e == cudaSuccess)
-        e = cider::launch_gemv(q, sa, M, N, K, w, false, sw, group_size, cider::kEpiY, yh, nullptr,
-                               sms, st);
+      e = cider::launch_gemv(static_cast<const __half*>(x), nullptr, nullptr, M, N, K, w, false, sw,
+                             group_size, cider::kEpiY, yh, nullptr, sms, st);
     } else {
       const size_t qbytes = round256(2 * static_cast<size_t>(M) * static_cast<size_t>(K));
       const size_t vbytes = round256(4 * static_cast<size_t>(M));

@@ -34,14 +34,12 @@ __device__ __forceinline__ float block_max_128(float v, float* red) {
   return v;
 }
 
-__device__ __forceinline__ float quant_code(float x, float s) {
-  float r = rintf(__fdiv_rn(x, s));
-  return fminf(fmaxf(r, -127.0f), 127.0f);
-}
+__device__ __forceinline__ float quant_code(float x, float s, float r) { return act_code(x, s, r); }
 
 // Eight fp16 values -> eight codes, stored as int8 (8 bytes) or as fp16
 // integers (16 bytes; exact, the operand format of the tensor-core GEMM).
-__device__ __forceinline__ int store_codes(int8_t* q, int64_t off, const uint4& v, float s) {
+__device__ __forceinline__ int store_codes(int8_t* q, int64_t off, const uint4& v, float s,
+                                           float r) {
   const __half2* h = reinterpret_cast<const __half2*>(&v);
   uint32_t w[2];
   int l1 = 0;
@@ -51,8 +49,8 @@ __device__ __forceinline__ int store_codes(int8_t* q, int64_t off, const uint4& 
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       float2 f = __half22float2(h[2 * j + e]);
-      int c0 = static_cast<int>(quant_code(f.x, s));
-      int c1 = static_cast<int>(quant_code(f.y, s));
+      int c0 = static_cast<int>(quant_code(f.x, s, r));
+      int c1 = static_cast<int>(quant_code(f.y, s, r));
       l1 += abs(c0) + abs(c1);
       b |= (static_cast<uint32_t>(c0 & 0xFF) << (16 * e)) |
            (static_cast<uint32_t>(c1 & 0xFF) << (16 * e + 8));
@@ -62,7 +60,8 @@ __device__ __forceinline__ int store_codes(int8_t* q, int64_t off, const uint4& 
   *reinterpret_cast<uint2*>(q + off) = make_uint2(w[0], w[1]);
   return l1;
 }
-__device__ __forceinline__ int store_codes(__half* q, int64_t off, const uint4& v, float s) {
+__device__ __forceinline__ int store_codes(__half* q, int64_t off, const uint4& v, float s,
+                                           float r) {
   const __half2* h = reinterpret_cast<const __half2*>(&v);
   uint4 o;
   uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
@@ -70,7 +69,7 @@ __device__ __forceinline__ int store_codes(__half* q, int64_t off, const uint4& 
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     float2 f = __half22float2(h[j]);
-    const float c0 = quant_code(f.x, s), c1 = quant_code(f.y, s);
+    const float c0 = quant_code(f.x, s, r), c1 = quant_code(f.y, s, r);
     l1 += fabsf(c0) + fabsf(c1);
     __half2 r = __floats2half2_rn(c0, c1);
     ow[j] = *reinterpret_cast<uint32_t*>(&r);
@@ -115,12 +114,13 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const __half* 
   float amax = fmaxf(__low2float(amax2), __high2float(amax2));
   amax = block_max_128(amax, red);
   const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
+  const float r = __frcp_rn(s);
   if (threadIdx.x == 0) sa[m] = s;
   int l1 = 0;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int idx = threadIdx.x + i * kQuantThreads;
-    if (idx < nvec) l1 += store_codes(q, m * K + static_cast<int64_t>(idx) * 8, v[i], s);
+    if (idx < nvec) l1 += store_codes(q, m * K + static_cast<int64_t>(idx) * 8, v[i], s, r);
   }
   if (row_l1 != nullptr) {
     l1 = block_sum_128(l1, ired);
@@ -151,10 +151,11 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_long_kernel(const __h
   float amax = fmaxf(__low2float(amax2), __high2float(amax2));
   amax = block_max_128(amax, red);
   const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
+  const float r = __frcp_rn(s);
   if (threadIdx.x == 0) sa[m] = s;
   int l1 = 0;
   for (int64_t idx = threadIdx.x; idx < nvec; idx += kQuantThreads)
-    l1 += store_codes(q, m * K + idx * 8, row[idx], s);
+    l1 += store_codes(q, m * K + idx * 8, row[idx], s, r);
   if (row_l1 != nullptr) {
     l1 = block_sum_128(l1, ired);
     if (threadIdx.x == 0) row_l1[m] = l1;
