@@ -166,6 +166,25 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
+def library_path(M: int, K: int, gs: int):
+    """(dominant kernel, kernel launches per step) of the library's dispatch for
+    one linear call: the same limits as gemv_fits() and launch_gemm_tc() in the
+    CUDA sources (small-M GEMV up to M=16 when its activation block and a ring
+    of at least four 4 KiB weight tiles fit in shared memory; otherwise the
+    per-token quantization kernel followed by one tensor-core GEMM)."""
+    if 1 <= M <= 16:
+        mb = 1
+        while mb < M:
+            mb *= 2
+        if mb * K <= 200 * 1024 and (227 * 1024 - 4096 - mb * K) // 4096 >= 4:
+            return "gemv_kernel (small-M weight-streaming GEMV, fused quantization)", 1
+    if gs:
+        return "gemm_tc_kernel (tcgen05 kind::f16 on exact integer codes, per-group epilogue)", 2
+    if K > 4096:
+        return "gemm_wide_kernel (tcgen05 kind::f16, weight operand in TMEM)", 2
+    return "gemm_wss_kernel (tcgen05 kind::f16, both operands in shared memory)", 2
+
+
 def ncu_traffic(workload: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, if it was taken on the current kernel source and workload."""
@@ -391,16 +410,18 @@ def run_ours(a):
         return
 
     peaks, peak_src = measured_peaks()
-    small_m = a.M <= 16
+    kernel_name, launches_per_step = library_path(a.M, a.K, a.gs)
+    small_m = launches_per_step == 1
     wl = workload_name(a)
     if small_m:
         wbytes = a.N * a.K if a.bits == 8 else a.N * a.K // 2
         G = a.K // a.gs if a.gs else 1
-        alg_bytes = wbytes + 4 * a.N * G + a.M * a.K + 4 * a.M + 2 * a.M * a.N
+        # the fused kernel reads x (fp16), the weight codes and scales, writes y
+        alg_bytes = wbytes + 4 * a.N * G + 2 * a.M * a.K + 2 * a.M * a.N
         achieved = alg_bytes / gemm_avg_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(wl),
-                "kernel": "gemv_kernel (small-M weight-streaming GEMV)",
+                "kernel": kernel_name,
                 "peak_source": f"{peak_src} hbm_gbs",
                 "algorithmic_bytes_per_launch": alg_bytes}
     else:
@@ -409,7 +430,7 @@ def run_ours(a):
         achieved = ops_step / gemm_avg_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
                 "frac": achieved / pk, "traffic": ncu_traffic(wl),
-                "kernel": "gemm_tc_kernel (tcgen05 kind::f16 on exact integer codes)",
+                "kernel": kernel_name,
                 "peak_source": (f"{peak_src} bf16_tflops"
                                 f"{'_sustained' if long_region else ''}"
                                 " x 1.0 (fp16 and bf16 dense tensor rates are equal)"),
@@ -429,7 +450,7 @@ def run_ours(a):
                    "launch": (f"CUDA graph of {per_graph} steps, replayed {a.steps // per_graph} times"
                               if graph is not None else "direct launches from Python")},
         "roofline": roof,
-        "gpu_launches": 2 * a.steps,
+        "gpu_launches": launches_per_step * a.steps,
         "e2e": e2e,
         "clocks": clk,
     }
