@@ -83,6 +83,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest of one float across all ranks (a no-op on one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tops(ops_per_rank_step: float, steps: int, world: int, elapsed_ms: float) -> float:
+    """Whole-job throughput: the work of all ranks over the slowest rank's time."""
+    return ops_per_rank_step * steps * world / (elapsed_ms * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples every 200 ms during the timed region."""
@@ -365,13 +381,10 @@ def run_ours(a):
     assert n_timed == (per_graph if graph is not None else a.steps), (n_timed, a.steps)
     if cider.cider_check_device_error() != 0:
         raise SystemExit("libcider reported a timed-out wait inside a kernel")
-    if ws > 1:
-        t = torch.tensor([el_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        el_ms = float(t.item())
+    el_ms = max_over_ranks(el_ms, dev)
 
     ops_step = 2.0 * a.M * a.N * a.K
-    value = ops_step * a.steps * ws / (el_ms * 1e-3) / 1e12
+    value = job_tops(ops_step, a.steps, ws, el_ms)
     gemm_avg_s = gemm_total_ms / n_timed * 1e-3
 
     # end to end through the public API with host buffers (copies inside the timed region)
@@ -396,11 +409,8 @@ def run_ours(a):
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": ops_step * n_e2e * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+    e2e_ms = max_over_ranks(e2e_ms, dev)
+    e2e = {"value": job_tops(ops_step, n_e2e, ws, e2e_ms), "unit": UNIT,
            "h2d_bytes_per_step": 2 * a.M * a.K, "d2h_bytes_per_step": 2 * a.M * a.N,
            "steps": n_e2e}
 

@@ -162,6 +162,16 @@ def test_full_size_sampled_rows(cider, M, N, K, gs, bits):
         assert_fp16_close(y[rows], yref, f"full-size rows M={M} N={N} K={K} gs={gs}")
 
 
+def test_single_layer_workload_all_rows(cider):
+    """The single W8A8 per-channel layer workload (x fp16 [128, 2560], W [2560,
+    2560], seed 0): every output against the oracle, bit for bit."""
+    M, N, K = 128, 2560, 2560
+    x, W = inputs.layer(M, N, K, base_seed=0, index=0)
+    qw, sw = oracle.quantize_weight_int8(W, 0)
+    y = run_linear(cider, x, qw, sw, 0, 8)
+    assert_bits_equal(y, oracle.linear(x, qw, sw, 0, threads=8), "single layer, all rows")
+
+
 def test_no_device_error_left(cider):
     assert cider.cider_check_device_error() == 0
 
