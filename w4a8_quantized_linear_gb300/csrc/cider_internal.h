@@ -66,6 +66,11 @@ cudaError_t launch_gemm_tc(const __half* qa16, const float* sa, const int* row_l
                            int64_t N, int64_t K, const uint8_t* w, bool int4, const float* sw,
                            int group_size, int mode, __half* y, int32_t* acc, int num_sms,
                            cudaStream_t st);
+// gemm_pair.cu: per-channel tensor-core path on CTA pairs (same operands as
+// launch_gemm_tc with group_size 0).
+cudaError_t launch_gemm_pair(const __half* qa16, const float* sa, const int* row_l1, int64_t M,
+                             int64_t N, int64_t K, const uint8_t* w, bool int4, const float* sw,
+                             int mode, __half* y, int32_t* acc, cudaStream_t st);
 cudaError_t read_and_clear_device_error(int* value);
 // Device address of the library's error word on the current device.
 cudaError_t device_error_word(int** ptr);

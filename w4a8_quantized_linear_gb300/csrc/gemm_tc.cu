@@ -1092,8 +1092,10 @@ cudaError_t launch_gemm_tc(const __half* qa16, const float* sa, const int* row_l
                            int64_t N, int64_t K, const uint8_t* w, bool int4, const float* sw,
                            int group_size, int mode, __half* y, int32_t* acc, int num_sms,
                            cudaStream_t st) {
+  if (group_size == 0 && row_l1 != nullptr)
+    return launch_gemm_pair(qa16, sa, row_l1, M, N, K, w, int4, sw, mode, y, acc, st);
   CUtensorMap tmA, tmB;
-  const bool wide = group_size == 0 && row_l1 != nullptr;
+  const bool wide = false;
   if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qa16, K, M, K * 2, kBK,
                    wide ? kWTileM : kTileM, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
