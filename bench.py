@@ -187,7 +187,8 @@ def library_path(M: int, K: int, gs: int):
     one linear call: the same limits as gemv_fits() and launch_gemm_tc() in the
     CUDA sources (small-M GEMV up to M=16 when its activation block and a ring
     of at least four 4 KiB weight tiles fit in shared memory; otherwise the
-    per-token quantization kernel followed by one tensor-core GEMM)."""
+    per-token quantization kernel, for per-channel problems with M >= 8192 a
+    weight conversion pass, and one tensor-core GEMM)."""
     if 1 <= M <= 16:
         mb = 1
         while mb < M:
@@ -196,9 +197,9 @@ def library_path(M: int, K: int, gs: int):
             return "gemv_kernel (small-M weight-streaming GEMV, fused quantization)", 1
     if gs:
         return "gemm_tc_kernel (tcgen05 kind::f16 on exact integer codes, per-group epilogue)", 2
-    if K > 4096:
-        return "gemm_wide_kernel (tcgen05 kind::f16, weight operand in TMEM)", 2
-    return "gemm_wss_kernel (tcgen05 kind::f16, both operands in shared memory)", 2
+    if M >= 8192:   # kPreconvMinM: weights converted to fp16 once per call
+        return ("gemm_pair_kernel (tcgen05 cta_group::2, 256x256 tiles, fp16 weights by TMA)", 3)
+    return "gemm_pair_kernel (tcgen05 cta_group::2, 256x256 tiles, in-kernel conversion)", 2
 
 
 def ncu_traffic(workload: str):

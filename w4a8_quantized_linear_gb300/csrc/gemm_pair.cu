@@ -9,53 +9,59 @@
 // below 2^24 (see the per-tile bound below).
 //
 // A cluster of two CTAs (on two SMs) computes a 256 x 256 output tile,
-// 256 weight rows (n) x 256 tokens (m), with tcgen05.mma.cta_group::2:
-// CTA r of the pair holds weight rows [128 r, 128 r + 128) of the tile (the
-// MMA's A operand, M = 256 split over the pair) and tokens [128 r, 128 r + 128)
+// 256 tokens (m) x 256 weight rows (n), with tcgen05.mma.cta_group::2:
+// CTA r of the pair holds tokens [128 r, 128 r + 128) of the tile (the MMA's
+// A operand, M = 256 split over the pair) and weight rows [128 r, 128 r + 128)
 // (its half of the B operand, N = 256); each CTA's tensor memory receives its
-// own 128 weight rows x all 256 tokens.  Per SM this halves the activation
-// bytes read from L2 and shared memory per multiply-add compared with a
-// 128 x 256 tile on one SM, which is what lets the tensor pipe run at its
-// full rate.
+// own 128 tokens (one per lane) x all 256 weight rows.  Per SM this halves
+// the operand bytes read per multiply-add compared with a 128 x 256 tile on
+// one SM, which is what lets the tensor pipe run at its full rate.
+//
+// Two ways to feed the weight operand (fp16, K-major, 128-byte swizzle):
+//   PRECONV   the weights were converted to fp16 in global memory by
+//             convert_weights_kernel before the GEMM (one streaming pass,
+//             amortised over all token tiles: the large-M choice); both
+//             operands arrive by TMA.
+//   otherwise converter warps turn the int8 / int4 codes of each stage into
+//             fp16 in shared memory (no extra pass or scratch: the small-M
+//             choice, and the allocation-free entry point's).
 //
 // Roles in each CTA (one CTA per SM, persistent over tiles):
-//   warp 0      activation producer: TMA of the CTA's fp16 codes [128 m][64 k]
-//               (128-byte swizzle) into the 6-stage operand ring; the copies
-//               of both CTAs complete on the even CTA's "ready" barrier.
-//   warp 14     weight producer: TMA of int8 codes [128 n][64 k] (64-byte
-//               swizzle; INT4: packed [128 n][32 B], 32-byte swizzle) into a
-//               separate 4-slot ring, running ahead of the conversion.
-//   warps 2-9   converters, two groups of 4 warps taking alternate stages:
-//               each thread owns one weight row, converts its 64 codes of the
-//               stage to fp16 and writes them into the stage's A operand in
-//               the canonical K-major 128-byte-swizzled layout as soon as the
-//               stage is free, then reports to the even CTA's "ready" barrier.
-//               (One group alone is latency-bound at ~450 ns per stage, the
-//               MMAs of a stage take ~250 ns.)
+//   warp 0      producer: TMA of the CTA's activation codes (fp16, two
+//               [128 m][64 k] sub-tiles per 128-K stage) and, PRECONV, its fp16
+//               weights (two [128 n][64 k]) into the 3-stage operand ring; the
+//               copies of both CTAs complete on the even CTA's "ready" barrier.
 //   warp 1      even CTA only, one thread: waits until both CTAs' stages are
-//               ready, issues 4 MMAs (K = 16 each) into one of two 256-column
-//               accumulators, and commits to both CTAs' barriers (stage free;
+//               ready, issues 8 MMAs (K = 16 each) into one of two 256-column
+//               accumulators and commits to both CTAs' barriers (stage free;
 //               accumulator full).  Both CTAs' warp 1 allocate tensor memory.
-//   warps 10-13 epilogue, one per tensor-memory lane quarter: drain the
-//               accumulator (tcgen05.ld), dequantize, store fp16 y (or int32
-//               accumulators), release it.
-// Keeping the int8 weights out of the operand ring leaves room for six
-// 32 KiB stages: enough work in flight to cover the ~2 us it takes to refill
-// a stage (commit, TMA from L2, conversion, cross-CTA signal).
+//               128-K stages halve the per-stage synchronisation cost, which
+//               with 64-K stages kept the tensor pipe ~30 % idle.
+//   epilogue    4 warps, one per tensor-memory lane quarter: drain the
+//               accumulator (tcgen05.ld: a thread holds 32 consecutive weight
+//               rows of its token), dequantize, store fp16 y with 16-byte
+//               stores (or int32 accumulators), release the accumulator.
+//   converters  (not PRECONV) two groups of 4 warps taking alternate stages:
+//               each thread converts its weight row's 128 codes of the stage
+//               (two 64-K sub-tiles) and writes them in the canonical K-major
+//               swizzled layout, then reports to the even CTA's "ready"
+//               barrier.
+//   w-producer  (not PRECONV) TMA of the int8 codes [128 n][64 k] (INT4:
+//               packed [128 n][32 B]) into a separate 4-slot ring, one
+//               sub-tile per slot, running ahead of the conversion.
 //
 // Exactness per tile: every partial sum of token m is bounded by
 // qmax_w * sum_k |q_a[m,k]| (qmax_w = 127 INT8, 8 INT4).  When that bound is
 // <= 2^23 for all 256 tokens of the tile ("fast" tile, the normal case) all of
 // K accumulates in fp32 exactly and the accumulator is drained once.  Else
-// ("slow" tile) the tile runs as four passes of 64 tokens (N = 64 MMAs, 32
-// tokens from each CTA) whose accumulators are drained every 512 K into exact
-// int32 register sums.
+// ("slow" tile) the tile runs as four passes of 64 weight rows (N = 64 MMAs,
+// 32 rows from each CTA) whose accumulators are drained every 512 K into
+// exact int32 register sums.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
 #include <atomic>
-#include <mutex>
 
 #include "cider_device.cuh"
 #include "cider_internal.h"
@@ -63,38 +69,46 @@
 namespace cider {
 namespace {
 
-constexpr int kPTileN = 256;          // weight rows per pair tile (MMA M)
-constexpr int kPTileM = 256;          // tokens per pair tile (MMA N)
+constexpr int kPTileM = 256;          // tokens per pair tile (MMA M, tensor-memory lanes)
+constexpr int kPTileN = 256;          // weight rows per pair tile (MMA N)
 constexpr int kPHalf = 128;           // rows of each operand per CTA
-constexpr int kPBK = 64;              // K per pipeline stage
+constexpr int kPSubK = 64;            // K per swizzled sub-tile (128 bytes of fp16)
+constexpr int kPSub = 2;              // sub-tiles per pipeline stage
+constexpr int kPBK = kPSub * kPSubK;  // K per pipeline stage: 8 MMAs
 constexpr int kPUmmaK = 16;
-constexpr int kPStages = 6;           // operand ring (activations + converted weights)
-constexpr int kP8Slots = 4;           // int8 / int4 weight ring
-constexpr int kPChunkKB = 8;          // slow tiles: drain every 512 K
-constexpr int kPThreads = 480;
-constexpr int kPConvWarp0 = 2;        // two groups of 4 converter warps
-constexpr int kPEpiWarp0 = 10;
-constexpr int kPSlowPasses = 4;       // slow tiles: 64 tokens per pass
-constexpr int kPW8Warp = 14;
+constexpr int kPChunkKB = 4;          // slow tiles: drain every 512 K
+constexpr int kPSlowPasses = 4;       // slow tiles: 64 weight rows per pass
 constexpr int kPAccCols = 256;
 constexpr int kPTmemCols = 512;
-constexpr int kPBBytes = kPHalf * kPBK * 2;    // 16 KiB activation codes
-constexpr int kPA16Bytes = kPHalf * kPBK * 2;  // 16 KiB converted weights
-constexpr int kPStageBytes = kPBBytes + kPA16Bytes;
+constexpr int kPSubBytes = kPHalf * kPSubK * 2;  // 16 KiB: one operand sub-tile, fp16
+constexpr int kPOpBytes = kPSub * kPSubBytes;    // 32 KiB: one operand of a stage
+constexpr int kPStageBytes = 2 * kPOpBytes;      // activations | weights
+constexpr int kP8Slots = 4;                      // int8 / int4 weight ring, one sub-tile per slot
 constexpr uint64_t kPWaitNs = 2000000000ull;
 
-template <bool INT4>
+template <bool INT4, bool PRECONV>
 struct PCfg {
-  static constexpr int kA8Bytes = INT4 ? kPHalf * kPBK / 2 : kPHalf * kPBK;
-  static constexpr int kA8Offset = kPStages * kPStageBytes;
-  static constexpr int kBarOffset = kA8Offset + kP8Slots * 8192;
+  static constexpr int kStages = 3;
+  static constexpr int kConvWarp0 = 2;
+  static constexpr int kConvWarps = PRECONV ? 0 : 8;
+  static constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;
+  static constexpr int kW8Warp = kEpiWarp0 + 4;  // only without PRECONV
+  static constexpr int kThreads = 32 * (PRECONV ? kEpiWarp0 + 4 : kW8Warp + 1);
+  static constexpr int kA8Bytes = INT4 ? kPHalf * kPSubK / 2 : kPHalf * kPSubK;
+  static constexpr int kA8Offset = kStages * kPStageBytes;
+  static constexpr int kBarOffset = kA8Offset + (PRECONV ? 0 : kP8Slots * 8192);
   // ready, empty per stage; full8, empty8 per weight slot; accf x2, acce x2,
-  // mma_done; tmem slot; abort
-  static constexpr int kNumBars = 2 * kPStages + 2 * kP8Slots + 5;
+  // mma_done; then the tensor-memory slot and the abort flag
+  static constexpr int kBar8 = 2 * kStages;
+  static constexpr int kBar2 = kBar8 + 2 * kP8Slots;
+  static constexpr int kNumBars = kBar2 + 5;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;
+  // the even CTA's producer arrival (+ 4 converter warps x 2 CTAs)
+  static constexpr int kReadyCount = PRECONV ? 1 : 9;
+  static constexpr uint32_t kReadyBytes = (PRECONV ? 4 : 2) * kPOpBytes;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
-static_assert(kPStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for the swizzle");
-static_assert(PCfg<false>::kSmemBytes <= 232448, "shared memory budget");
+static_assert(kPSubBytes % 1024 == 0, "sub-tiles must keep 1024-byte alignment for the swizzle");
 
 struct PairArgs {
   int M, N, K;
@@ -120,30 +134,46 @@ __device__ __forceinline__ bool pair_tile_fast(const PairArgs& a, int mt, int la
   return mx <= a.l1_limit;
 }
 
-template <bool INT4, int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
-    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+// y[m, n0 .. n0 + 7] = fp16((acc * s_a[m]) * s_w[n]) from eight exact
+// accumulator values, one 16-byte store.
+__device__ __forceinline__ void store8_y(const PairArgs& p, int m, float sam, int n0, const float* f) {
+  uint32_t h[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half lo = __float2half_rn(__fmul_rn(__fmul_rn(f[2 * i], sam), __ldg(p.sw + n0 + 2 * i)));
+    const __half hi =
+        __float2half_rn(__fmul_rn(__fmul_rn(f[2 * i + 1], sam), __ldg(p.sw + n0 + 2 * i + 1)));
+    h[i] = static_cast<uint32_t>(__half_as_ushort(lo)) |
+           (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+  }
+  *reinterpret_cast<uint4*>(p.y + static_cast<int64_t>(m) * p.N + n0) =
+      make_uint4(h[0], h[1], h[2], h[3]);
+}
+
+template <bool INT4, int EPI, bool PRECONV>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PCfg<INT4, PRECONV>::kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const PairArgs p) {
-  using C = PCfg<INT4>;
+  using C = PCfg<INT4, PRECONV>;
+  constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  auto sB = [&](int s) { return base + s * kPStageBytes; };
-  auto sA16 = [&](int s) { return base + s * kPStageBytes + kPBBytes; };
-  auto sA8 = [&](int j) { return base + C::kA8Offset + j * 8192; };
+  auto sA = [&](int s) { return base + s * kPStageBytes; };               // activation codes
+  auto sB = [&](int s) { return base + s * kPStageBytes + kPOpBytes; };   // fp16 weights
+  auto sW8 = [&](int j) { return base + C::kA8Offset + j * 8192; };
   const uint32_t bars = base + C::kBarOffset;
   auto ready_bar = [&](int s) { return bars + 8u * s; };
-  auto empty_bar = [&](int s) { return bars + 8u * (kPStages + s); };
-  auto full8_bar = [&](int j) { return bars + 8u * (2 * kPStages + j); };
-  auto empty8_bar = [&](int j) { return bars + 8u * (2 * kPStages + kP8Slots + j); };
-  constexpr int kBar2 = 2 * kPStages + 2 * kP8Slots;
-  auto accf_bar = [&](int b) { return bars + 8u * (kBar2 + b); };
-  auto acce_bar = [&](int b) { return bars + 8u * (kBar2 + 2 + b); };
-  const uint32_t done_bar = bars + 8u * (kBar2 + 4);
-  const uint32_t tmem_slot = bars + 8u * (kBar2 + 5);
+  auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+  auto full8_bar = [&](int j) { return bars + 8u * (C::kBar8 + j); };
+  auto empty8_bar = [&](int j) { return bars + 8u * (C::kBar8 + kP8Slots + j); };
+  auto accf_bar = [&](int b) { return bars + 8u * (C::kBar2 + b); };
+  auto acce_bar = [&](int b) { return bars + 8u * (C::kBar2 + 2 + b); };
+  const uint32_t done_bar = bars + 8u * (C::kBar2 + 4);
+  const uint32_t tmem_slot = bars + 8u * C::kNumBars;
   volatile uint32_t* abort_flag =
-      reinterpret_cast<volatile uint32_t*>(gbase + C::kBarOffset + 8 * (kBar2 + 5) + 4);
+      reinterpret_cast<volatile uint32_t*>(gbase + C::kBarOffset + 8 * C::kNumBars + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -153,15 +183,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   int* err = p.err;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kPStages; ++s) {
-      // the even CTA's producer arrival (with the byte count of both CTAs'
-      // activation copies) + 4 converter warps x 2 CTAs
-      mbar_init(ready_bar(s), 9);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(ready_bar(s), C::kReadyCount);
       mbar_init(empty_bar(s), 1);
     }
-    for (int j = 0; j < kP8Slots; ++j) {
-      mbar_init(full8_bar(j), 1);
-      mbar_init(empty8_bar(j), 4);     // the 4 warps of the converter group of this use
+    if (!PRECONV) {
+      for (int j = 0; j < kP8Slots; ++j) {
+        mbar_init(full8_bar(j), 1);
+        mbar_init(empty8_bar(j), 4);   // the 4 warps of the converter group of this use
+      }
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -171,8 +201,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     *abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) prefetch_tensormap(&tmB);
-  if (warp == kPW8Warp && lane == 0) prefetch_tensormap(&tmA);
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmX);
+    prefetch_tensormap(&tmW);
+  }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, kPTmemCols);
     tmem_relinquish_pair();
@@ -181,34 +213,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   __syncthreads();
   cluster_sync_all();   // barriers of both CTAs initialised, tensor memory held
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + C::kBarOffset +
-                                                              8 * (kBar2 + 5));
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + C::kBarOffset + 8 * C::kNumBars);
   const int nkb = (p.K + kPBK - 1) / kPBK;
   const int nch = (nkb + kPChunkKB - 1) / kPChunkKB;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ activation producer
+    // ------------------------------------------------------------ producer
     const uint32_t ready_leader0 = mapa_shared(ready_bar(0), 0);
-    int it = 0;
-    for (int tile = cid; tile < p.num_tiles; tile += nclusters) {
-      const int mt = tile % p.num_m_tiles;
-      const int passes = pair_tile_fast(p, mt, lane) ? 1 : kPSlowPasses;
-      if (lane == 0) {
-        for (int pass = 0; pass < passes; ++pass)
-          for (int kb = 0; kb < nkb; ++kb, ++it) {
-            const int s = it % kPStages;
-            const uint32_t ph = (it / kPStages) & 1;
-            if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, err, kPWaitNs)) break;
-            if (rank == 0) mbar_arrive_expect_tx(ready_bar(s), 2 * kPBBytes);
-            tma_load_2d_pair(sB(s), &tmB, ready_leader0 + 8u * s, kb * kPBK,
-                             mt * kPTileM + rank * kPHalf);
-          }
-      }
-      __syncwarp();
-      if (*abort_flag) break;
-    }
-  } else if (warp == kPW8Warp) {
-    // ------------------------------------------------------------ weight producer
     int it = 0;
     for (int tile = cid; tile < p.num_tiles; tile += nclusters) {
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
@@ -216,12 +227,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       if (lane == 0) {
         for (int pass = 0; pass < passes; ++pass)
           for (int kb = 0; kb < nkb; ++kb, ++it) {
-            const int j = it % kP8Slots;
-            const uint32_t ph = (it / kP8Slots) & 1;
-            if (!mbar_wait_bounded(empty8_bar(j), ph ^ 1u, abort_flag, err, kPWaitNs)) break;
-            mbar_arrive_expect_tx(full8_bar(j), C::kA8Bytes);
-            tma_load_2d(sA8(j), &tmA, full8_bar(j), INT4 ? kb * (kPBK / 2) : kb * kPBK,
-                        nt * kPTileN + rank * kPHalf);
+            const int s = it % S;
+            const uint32_t ph = (it / S) & 1;
+            if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, err, kPWaitNs)) break;
+            if (rank == 0) mbar_arrive_expect_tx(ready_bar(s), C::kReadyBytes);
+            for (int t = 0; t < kPSub; ++t) {
+              const int k0 = kb * kPBK + t * kPSubK;
+              tma_load_2d_pair(sA(s) + t * kPSubBytes, &tmX, ready_leader0 + 8u * s, k0,
+                               mt * kPTileM + rank * kPHalf);
+              if (PRECONV)
+                tma_load_2d_pair(sB(s) + t * kPSubBytes, &tmW, ready_leader0 + 8u * s, k0,
+                                 nt * kPTileN + rank * kPHalf);
+            }
           }
       }
       __syncwarp();
@@ -230,8 +247,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (rank == 0) {
-      constexpr uint32_t idesc_fast = idesc_f16_f32(kPTileN, kPTileM);
-      constexpr uint32_t idesc_slow = idesc_f16_f32(kPTileN, kPTileM / kPSlowPasses);
+      constexpr uint32_t idesc_fast = idesc_f16_f32(kPTileM, kPTileN);
+      constexpr uint32_t idesc_slow = idesc_f16_f32(kPTileM, kPTileN / kPSlowPasses);
       int it = 0, ch = 0;
       for (int tile = cid; tile < p.num_tiles; tile += nclusters) {
         const int mt = tile % p.num_m_tiles;
@@ -251,21 +268,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
               }
-              const int s = it % kPStages;
-              const uint32_t ph = (it / kPStages) & 1;
+              const int s = it % S;
+              const uint32_t ph = (it / S) & 1;
               if (!mbar_wait_bounded(ready_bar(s), ph, abort_flag, err, kPWaitNs)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              const uint64_t adesc = smem_desc_k_sw128(sA16(s));
-              // slow pass p uses rows [32 p, 32 p + 32) of each CTA's 128 tokens
+              const uint64_t adesc = smem_desc_k_sw128(sA(s));
+              // slow pass p uses weight rows [32 p, 32 p + 32) of each CTA's 128
               const uint64_t bdesc = smem_desc_k_sw128(sB(s) + (fast ? 0 : pass * (32 * 128)));
 #pragma unroll
-              for (int j = 0; j < kPBK / kPUmmaK; ++j)
-                tc_mma_ss_pair(tmem + b * kPAccCols, adesc + static_cast<uint64_t>(j * 2),
-                               bdesc + static_cast<uint64_t>(j * 2), fast ? idesc_fast : idesc_slow,
-                               (cstart && j == 0) ? 0u : 1u);
+              for (int j = 0; j < kPBK / kPUmmaK; ++j) {
+                // sub-tile j / 4, K step j % 4 (+32 bytes each) inside it
+                const uint64_t off = static_cast<uint64_t>((j >> 2) * (kPSubBytes >> 4) + (j & 3) * 2);
+                tc_mma_ss_pair(tmem + b * kPAccCols, adesc + off, bdesc + off,
+                               fast ? idesc_fast : idesc_slow, (cstart && j == 0) ? 0u : 1u);
+              }
               tc_commit_pair_mc(empty_bar(s), 0x3);
               if (cend) {
                 tc_commit_pair_mc(accf_bar(b), 0x3);
@@ -282,9 +301,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       if (lane == 0) tc_commit_pair_mc(done_bar, 0x3);
       __syncwarp();
     }
-  } else if (warp < kPEpiWarp0) {
+  } else if (!PRECONV && warp < C::kEpiWarp0) {
     // ------------------------------------------------------------ converters
-    const int group = (warp - kPConvWarp0) >> 2;   // takes the uses with it % 2 == group
+    const int group = (warp - C::kConvWarp0) >> 2;   // takes the uses with it % 2 == group
     const int row = (warp & 3) * 32 + lane;
     const uint32_t ready_leader0 = mapa_shared(ready_bar(0), 0);
     int it = 0;
@@ -294,96 +313,129 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       for (int pass = 0; pass < passes; ++pass) {
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           if ((it & 1) != group) continue;
-          const int j8 = it % kP8Slots;
-          const uint32_t ph8 = (it / kP8Slots) & 1;
-          if (!__all_sync(0xffffffffu, mbar_wait_bounded(full8_bar(j8), ph8, abort_flag, err,
-                                                         kPWaitNs)))
-            goto done;
-          uint32_t h[32];
-          const uint8_t* arow = gbase + (sA8(j8) - base);
-          if (!INT4) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1;
+          uint8_t* drow = gbase + (sB(s) - base) + row * 128;
+#pragma unroll 1
+          for (int t = 0; t < kPSub; ++t) {
+            const int v8 = it * kPSub + t;   // weight sub-tile index
+            const int j8 = v8 % kP8Slots;
+            const uint32_t ph8 = (v8 / kP8Slots) & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(full8_bar(j8), ph8, abort_flag, err,
+                                                           kPWaitNs)))
+              goto done;
+            uint32_t h[32];
+            const uint8_t* arow = gbase + (sW8(j8) - base);
+            if (!INT4) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const uint4 v = *reinterpret_cast<const uint4*>(
-                  arow + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
-              s8x4_to_h2x2(v.x, h[8 * c + 0], h[8 * c + 1]);
-              s8x4_to_h2x2(v.y, h[8 * c + 2], h[8 * c + 3]);
-              s8x4_to_h2x2(v.z, h[8 * c + 4], h[8 * c + 5]);
-              s8x4_to_h2x2(v.w, h[8 * c + 6], h[8 * c + 7]);
-            }
-          } else {
+              for (int c = 0; c < 4; ++c) {
+                const uint4 v = *reinterpret_cast<const uint4*>(
+                    arow + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
+                s8x4_to_h2x2(v.x, h[8 * c + 0], h[8 * c + 1]);
+                s8x4_to_h2x2(v.y, h[8 * c + 2], h[8 * c + 3]);
+                s8x4_to_h2x2(v.z, h[8 * c + 4], h[8 * c + 5]);
+                s8x4_to_h2x2(v.w, h[8 * c + 6], h[8 * c + 7]);
+              }
+            } else {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const uint4 v = *reinterpret_cast<const uint4*>(
-                  arow + row * 32 + ((c ^ ((row >> 2) & 1)) << 4));
-              const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+              for (int c = 0; c < 2; ++c) {
+                const uint4 v = *reinterpret_cast<const uint4*>(
+                    arow + row * 32 + ((c ^ ((row >> 2) & 1)) << 4));
+                const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t t[4];
-                s4x8_to_h2x4(vw[q4], t);
-                h[16 * c + 4 * q4 + 0] = t[0];
-                h[16 * c + 4 * q4 + 1] = t[1];
-                h[16 * c + 4 * q4 + 2] = t[2];
-                h[16 * c + 4 * q4 + 3] = t[3];
+                for (int q4 = 0; q4 < 4; ++q4) {
+                  uint32_t tt[4];
+                  s4x8_to_h2x4(vw[q4], tt);
+                  h[16 * c + 4 * q4 + 0] = tt[0];
+                  h[16 * c + 4 * q4 + 1] = tt[1];
+                  h[16 * c + 4 * q4 + 2] = tt[2];
+                  h[16 * c + 4 * q4 + 3] = tt[3];
+                }
               }
             }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(empty8_bar(j8));   // weight slot consumed (in registers)
-          // the stage's A operand is free once the MMAs of its previous use completed
-          const int s = it % kPStages;
-          const uint32_t ph = (it / kPStages) & 1;
-          if (!__all_sync(0xffffffffu, mbar_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, err,
-                                                         kPWaitNs)))
-            goto done;
-          uint8_t* drow = gbase + (sA16(s) - base) + row * 128;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty8_bar(j8));   // weight slot consumed (in registers)
+            // the stage's weight operand is free once the MMAs of its previous use completed
+            if (t == 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(empty_bar(s), ph ^ 1u,
+                                                                     abort_flag, err, kPWaitNs)))
+              goto done;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(drow + ((c ^ (row & 7)) << 4)) =
-                make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(drow + t * kPSubBytes + ((c ^ (row & 7)) << 4)) =
+                  make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive_remote(ready_leader0 + 8u * s);
         }
       }
     }
-  } else if (warp < kPW8Warp) {
+  } else if (!PRECONV && warp == C::kW8Warp) {
+    // ------------------------------------------------------------ weight-code producer
+    int it = 0;
+    for (int tile = cid; tile < p.num_tiles; tile += nclusters) {
+      const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
+      const int passes = pair_tile_fast(p, mt, lane) ? 1 : kPSlowPasses;
+      if (lane == 0) {
+        bool ok = true;
+        for (int pass = 0; pass < passes && ok; ++pass)
+          for (int kb = 0; kb < nkb && ok; ++kb)
+            for (int t = 0; t < kPSub; ++t, ++it) {
+              const int j = it % kP8Slots;
+              const uint32_t ph = (it / kP8Slots) & 1;
+              if (!mbar_wait_bounded(empty8_bar(j), ph ^ 1u, abort_flag, err, kPWaitNs)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(full8_bar(j), C::kA8Bytes);
+              const int k0 = kb * kPBK + t * kPSubK;
+              tma_load_2d(sW8(j), &tmW, full8_bar(j), INT4 ? k0 / 2 : k0,
+                          nt * kPTileN + rank * kPHalf);
+            }
+      }
+      __syncwarp();
+      if (*abort_flag) break;
+    }
+  } else if (warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + 4) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // tensor-memory lane quarter of this warp
-    const int row = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
     int ch = 0;
     for (int tile = cid; tile < p.num_tiles; tile += nclusters) {
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
       const bool fast = pair_tile_fast(p, mt, lane);
-      const int n = nt * kPTileN + static_cast<int>(rank) * kPHalf + row;
-      const bool nvalid = n < p.N;
-      const float swn = (EPI == kEpiY && nvalid) ? __ldg(p.sw + n) : 0.0f;
+      const int m = mt * kPTileM + static_cast<int>(rank) * kPHalf + q * 32 + lane;
+      const bool mvalid = m < p.M;
+      const float sam = (EPI == kEpiY && mvalid) ? __ldg(p.sa + m) : 0.0f;
+      const int n_tile = nt * kPTileN;
       if (fast) {
         const int b = ch & 1;
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(accf_bar(b), (ch >> 1) & 1, abort_flag, err,
                                                        kPWaitNs)))
           goto done;
         tc_fence_after();
-        // column j of the accumulator is token mt * 256 + j
-        const int m0 = mt * kPTileM;
+        // column j of the accumulator is weight row nt * 256 + j
 #pragma unroll 1
         for (int c8 = 0; c8 < kPAccCols / 32; ++c8) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + b * kPAccCols + c8 * 32, v);
           tmem_wait_ld();
-          if (nvalid) {
+          if (mvalid) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int m = m0 + c8 * 32 + j;
-              if (m < p.M) {
-                const int64_t off = static_cast<int64_t>(m) * p.N + n;
-                const float f = __uint_as_float(v[j]);  // an exact integer
-                if (EPI == kEpiAcc)
-                  p.acc[off] = __float2int_rn(f);
-                else
-                  p.y[off] = __float2half_rn(__fmul_rn(__fmul_rn(f, __ldg(p.sa + m)), swn));
+            for (int g = 0; g < 4; ++g) {
+              const int n0 = n_tile + c8 * 32 + g * 8;
+              if (n0 < p.N) {   // N % 8 == 0: a group of 8 is all in or all out
+                if (EPI == kEpiAcc) {
+                  const int64_t off = static_cast<int64_t>(m) * p.N + n0;
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) p.acc[off + i] = __float2int_rn(__uint_as_float(v[g * 8 + i]));
+                } else {
+                  float f[8];
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v[g * 8 + i]);  // exact integers
+                  store8_y(p, m, sam, n0, f);
+                }
               }
             }
           }
@@ -415,18 +467,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(acce_leader0 + 8u * b);
           }
-          if (!nvalid) continue;
-          // N = 64 pass: column j is row 32 pass + (j % 32) of the tokens of CTA j / 32
+          if (!mvalid) continue;
+          // N = 64 pass: column j is weight row 32 pass + (j % 32) of CTA j / 32's 128
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const int m = mt * kPTileM + (j >> 5) * kPHalf + pass * 32 + (j & 31);
-            if (m < p.M) {
-              const int64_t off = static_cast<int64_t>(m) * p.N + n;
-              if (EPI == kEpiAcc)
-                p.acc[off] = isum[j];
-              else
-                p.y[off] = __float2half_rn(
-                    __fmul_rn(__fmul_rn(__int2float_rn(isum[j]), __ldg(p.sa + m)), swn));
+          for (int g = 0; g < 8; ++g) {
+            const int n0 = n_tile + (g >> 2) * kPHalf + pass * 32 + (g & 3) * 8;
+            if (n0 < p.N) {
+              if (EPI == kEpiAcc) {
+                const int64_t off = static_cast<int64_t>(m) * p.N + n0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) p.acc[off + i] = isum[g * 8 + i];
+              } else {
+                float f[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[i] = __int2float_rn(isum[g * 8 + i]);
+                store8_y(p, m, sam, n0, f);
+              }
             }
           }
         }
@@ -454,13 +510,48 @@ done:
   }
 }
 
-template <bool INT4, int EPI>
-cudaError_t launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const PairArgs& a,
+// int8 (or packed int4) weight codes [N, K] -> exact fp16 values [N, K]; one
+// thread per 16 consecutive values.
+template <bool INT4>
+__global__ void __launch_bounds__(256) convert_weights_kernel(const uint8_t* __restrict__ w,
+                                                              int64_t units, __half* __restrict__ out) {
+  for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < units;
+       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    uint32_t h[8];
+    if (!INT4) {
+      const uint4 v = ld_stream_v4(w + u * 16);
+      s8x4_to_h2x2(v.x, h[0], h[1]);
+      s8x4_to_h2x2(v.y, h[2], h[3]);
+      s8x4_to_h2x2(v.z, h[4], h[5]);
+      s8x4_to_h2x2(v.w, h[6], h[7]);
+    } else {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(w + u * 8));
+      uint32_t t[4];
+      s4x8_to_h2x4(v.x, t);
+      h[0] = t[0];
+      h[1] = t[1];
+      h[2] = t[2];
+      h[3] = t[3];
+      s4x8_to_h2x4(v.y, t);
+      h[4] = t[0];
+      h[5] = t[1];
+      h[6] = t[2];
+      h[7] = t[3];
+    }
+    uint4* o = reinterpret_cast<uint4*>(out + u * 16);
+    o[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    o[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
+template <bool INT4, int EPI, bool PRECONV>
+cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmW, const PairArgs& a,
                         cudaStream_t st) {
-  auto kern = gemm_pair_kernel<INT4, EPI>;
+  using C = PCfg<INT4, PRECONV>;
+  auto kern = gemm_pair_kernel<INT4, EPI, PRECONV>;
   static std::atomic<uint64_t> attr_done{0};
-  cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern),
-                                          PCfg<INT4>::kSmemBytes, attr_done);
+  cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::kSmemBytes,
+                                          attr_done);
   if (e != cudaSuccess) return e;
   // clusters that fit on the GPU at once (one CTA per SM), cached per device
   static std::atomic<int> max_clusters[64];
@@ -474,8 +565,8 @@ cudaError_t launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const Pa
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
-    cfg.blockDim = dim3(kPThreads, 1, 1);
-    cfg.dynamicSmemBytes = PCfg<INT4>::kSmemBytes;
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
     int q = 0;
     if (cudaOccupancyMaxActiveClusters(&q, reinterpret_cast<const void*>(kern), &cfg) !=
             cudaSuccess ||
@@ -487,24 +578,52 @@ cudaError_t launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const Pa
     if (dev < 64) max_clusters[dev].store(nc, std::memory_order_relaxed);
   }
   const int clusters = a.num_tiles < nc ? a.num_tiles : nc;
-  kern<<<2 * clusters, kPThreads, PCfg<INT4>::kSmemBytes, st>>>(tmA, tmB, a);
+  kern<<<2 * clusters, C::kThreads, C::kSmemBytes, st>>>(tmX, tmW, a);
   return cudaGetLastError();
+}
+
+template <bool INT4, int EPI>
+cudaError_t launch_pair_any(const CUtensorMap& tmX, const CUtensorMap& tmW, const PairArgs& a,
+                            bool preconv, cudaStream_t st) {
+  return preconv ? launch_pair<INT4, EPI, true>(tmX, tmW, a, st)
+                 : launch_pair<INT4, EPI, false>(tmX, tmW, a, st);
 }
 
 }  // namespace
 
+cudaError_t launch_convert_weights(const uint8_t* w, int64_t N, int64_t K, bool int4, __half* out,
+                                   int num_sms, cudaStream_t st) {
+  const int64_t units = N * K / 16;
+  int64_t blocks = (units + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (int4)
+    convert_weights_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, st>>>(w, units, out);
+  else
+    convert_weights_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(w, units, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gemm_pair(const __half* qa16, const float* sa, const int* row_l1, int64_t M,
-                             int64_t N, int64_t K, const uint8_t* w, bool int4, const float* sw,
-                             int mode, __half* y, int32_t* acc, cudaStream_t st) {
-  CUtensorMap tmA, tmB;
-  if (!make_tensor_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qa16, K, M, K * 2, kPBK, kPHalf,
+                             int64_t N, int64_t K, const uint8_t* w, bool int4, const __half* w16,
+                             const float* sw, int mode, __half* y, int32_t* acc, cudaStream_t st) {
+  CUtensorMap tmX, tmW;
+  if (!make_tensor_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qa16, K, M, K * 2, kPSubK, kPHalf,
                           CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  const uint64_t wbytes = int4 ? K / 2 : K;
-  if (!make_tensor_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, wbytes, N, wbytes,
-                          int4 ? kPBK / 2 : kPBK, kPHalf,
-                          int4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B))
-    return cudaErrorInvalidValue;
+  const bool preconv = w16 != nullptr;
+  if (preconv) {
+    if (!make_tensor_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, w16, K, N, K * 2, kPSubK, kPHalf,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  } else {
+    const uint64_t wbytes = int4 ? K / 2 : K;
+    if (!make_tensor_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, wbytes, N, wbytes,
+                            int4 ? kPSubK / 2 : kPSubK, kPHalf,
+                            int4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+  }
   PairArgs a;
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
@@ -520,10 +639,10 @@ cudaError_t launch_gemm_pair(const __half* qa16, const float* sa, const int* row
   cudaError_t e = device_error_word(&a.err);
   if (e != cudaSuccess) return e;
   if (int4)
-    return mode == kEpiY ? launch_pair<true, kEpiY>(tmA, tmB, a, st)
-                         : launch_pair<true, kEpiAcc>(tmA, tmB, a, st);
-  return mode == kEpiY ? launch_pair<false, kEpiY>(tmA, tmB, a, st)
-                       : launch_pair<false, kEpiAcc>(tmA, tmB, a, st);
+    return mode == kEpiY ? launch_pair_any<true, kEpiY>(tmX, tmW, a, preconv, st)
+                         : launch_pair_any<true, kEpiAcc>(tmX, tmW, a, preconv, st);
+  return mode == kEpiY ? launch_pair_any<false, kEpiY>(tmX, tmW, a, preconv, st)
+                       : launch_pair_any<false, kEpiAcc>(tmX, tmW, a, preconv, st);
 }
 
 }  // namespace cider
