@@ -226,18 +226,16 @@ cider_status_t run_linear(const LinearArgs& a) {
                                 a.int4, a.sw, gs, a.mode, y, a.acc, sms, a.st);
     }));
   }
-  // tensor-core path: activation codes as fp16 integers, scales, row sums of
-  // |code|, and for large per-channel problems the weights as fp16
+  // tensor-core path: activation codes as fp16 integers, scales, row sums of |code|
   const size_t qbytes = round_up(static_cast<size_t>(a.M * a.K) * 2, 256);
   const size_t vbytes = round_up(4 * a.M, 256);
-  const bool preconv = gs == 0 && a.M >= cider::kPreconvMinM;
-  const size_t wbytes = preconv ? round_up(static_cast<size_t>(a.N * a.K) * 2, 256) : 0;
-  cudaError_t e = scratch_alloc(scratch, dev, qbytes + 2 * vbytes + wbytes, a.st);
+  const size_t wsbytes = cider::gemm_tc_workspace_bytes(a.M, a.N, a.K, gs);
+  cudaError_t e = scratch_alloc(scratch, dev, qbytes + 2 * vbytes + wsbytes, a.st);
   if (e != cudaSuccess) return cuda_status(e);
   uint8_t* sbase = static_cast<uint8_t*>(scratch.ptr);
   __half* q16 = reinterpret_cast<__half*>(sbase);
   int* row_l1 = reinterpret_cast<int*>(sbase + qbytes + vbytes);
-  __half* w16 = preconv ? reinterpret_cast<__half*>(sbase + qbytes + 2 * vbytes) : nullptr;
+  void* ws = wsbytes ? sbase + qbytes + 2 * vbytes : nullptr;
   const float* sa = a.sa;
   if (a.x) {
     float* sscr = reinterpret_cast<float*>(sbase + qbytes);
@@ -248,13 +246,9 @@ cider_status_t run_linear(const LinearArgs& a) {
     e = cider::launch_codes_s8_to_f16(a.qa, a.M, a.K, q16, row_l1, a.st);
   }
   if (e != cudaSuccess) return cuda_status(e);
-  if (w16) {
-    e = cider::launch_convert_weights(w, a.N, a.K, a.int4, w16, sms, a.st);
-    if (e != cudaSuccess) return cuda_status(e);
-  }
   return cuda_status(timed_launch(a.st, [&] {
-    return cider::launch_gemm_tc(q16, sa, row_l1, a.M, a.N, a.K, w, a.int4, w16, a.sw, gs, a.mode,
-                                 y, a.acc, sms, a.st);
+    return cider::launch_gemm_tc(q16, sa, row_l1, a.M, a.N, a.K, w, a.int4, a.sw, gs, a.mode, y,
+                                 a.acc, ws, sms, a.st);
   }));
 }
 

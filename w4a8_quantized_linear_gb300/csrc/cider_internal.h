@@ -62,25 +62,19 @@ cudaError_t launch_gemv(const __half* x, const int8_t* qa, const float* sa, int6
 // gemm_tc.cu: tensor-core path.  qa16 holds the activation codes as fp16
 // integers [M, K]; row_l1[m] = sum_k |code| (used by the per-channel kernel
 // to decide per tile whether one fp32 accumulation over all of K is exact).
-// Per channel (group_size 0) it runs the CTA-pair kernel, reading the weights
-// from w16 (fp16 [N, K], written by launch_convert_weights) when w16 is not
-// null and converting the codes of w in the kernel otherwise.
+// Per channel (group_size 0) it runs the CTA-pair kernel of gemm_pair.cu,
+// split over K when the output tiles cannot occupy the GPU and `workspace`
+// (gemm_tc_workspace_bytes(...) bytes, or null to never split) allows it.
+size_t gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size);
 cudaError_t launch_gemm_tc(const __half* qa16, const float* sa, const int* row_l1, int64_t M,
-                           int64_t N, int64_t K, const uint8_t* w, bool int4, const __half* w16,
-                           const float* sw, int group_size, int mode, __half* y, int32_t* acc,
+                           int64_t N, int64_t K, const uint8_t* w, bool int4, const float* sw,
+                           int group_size, int mode, __half* y, int32_t* acc, void* workspace,
                            int num_sms, cudaStream_t st);
 // gemm_pair.cu: per-channel tensor-core path on CTA pairs (see launch_gemm_tc).
+size_t gemm_pair_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_pair(const __half* qa16, const float* sa, const int* row_l1, int64_t M,
-                             int64_t N, int64_t K, const uint8_t* w, bool int4, const __half* w16,
-                             const float* sw, int mode, __half* y, int32_t* acc, cudaStream_t st);
-// int8 (or packed int4) weight codes [N, K] -> exact fp16 values [N, K].
-cudaError_t launch_convert_weights(const uint8_t* w, int64_t N, int64_t K, bool int4, __half* out,
-                                   int num_sms, cudaStream_t st);
-// Smallest M for which the per-channel path converts the weights to fp16 once
-// per call (one streaming pass, ~17 us for 26 M int8 weights on GB300) instead
-// of once per 256-token tile inside the GEMM.  Measured on GB300 at N = 10240,
-// K = 2560: equal at M = 4096, 5 % faster at M = 8192.
-constexpr int64_t kPreconvMinM = 8192;
+                             int64_t N, int64_t K, const uint8_t* w, bool int4, const float* sw,
+                             int mode, __half* y, int32_t* acc, void* workspace, cudaStream_t st);
 cudaError_t read_and_clear_device_error(int* value);
 // Device address of the library's error word on the current device.
 cudaError_t device_error_word(int** ptr);

@@ -17,38 +17,42 @@
 // the operand bytes read per multiply-add compared with a 128 x 256 tile on
 // one SM, which is what lets the tensor pipe run at its full rate.
 //
-// Two ways to feed the weight operand (fp16, K-major, 128-byte swizzle):
-//   PRECONV   the weights were converted to fp16 in global memory by
-//             convert_weights_kernel before the GEMM (one streaming pass,
-//             amortised over all token tiles: the large-M choice); both
-//             operands arrive by TMA.
-//   otherwise converter warps turn the int8 / int4 codes of each stage into
-//             fp16 in shared memory (no extra pass or scratch: the small-M
-//             choice, and the allocation-free entry point's).
+// The weight operand (fp16, K-major, 128-byte swizzle) is made in shared
+// memory by converter warps from the int8 / int4 codes of each stage.
+// (Converting all weights to fp16 in global memory first and feeding both
+// operands by TMA makes the GEMM itself ~4 % faster on GB300, but the extra
+// streaming pass costs more than that at every measured shape.)
 //
 // Roles in each CTA (one CTA per SM, persistent over tiles):
 //   warp 0      producer: TMA of the CTA's activation codes (fp16, two
-//               [128 m][64 k] sub-tiles per 128-K stage) and, PRECONV, its fp16
-//               weights (two [128 n][64 k]) into the 3-stage operand ring; the
-//               copies of both CTAs complete on the even CTA's "ready" barrier.
+//               [128 m][64 k] sub-tiles per 128-K stage) into the 3-stage
+//               operand ring; the copies of both CTAs complete on the even
+//               CTA's "ready" barrier.
 //   warp 1      even CTA only, one thread: waits until both CTAs' stages are
 //               ready, issues 8 MMAs (K = 16 each) into one of two 256-column
 //               accumulators and commits to both CTAs' barriers (stage free;
 //               accumulator full).  Both CTAs' warp 1 allocate tensor memory.
 //               128-K stages halve the per-stage synchronisation cost, which
 //               with 64-K stages kept the tensor pipe ~30 % idle.
-//   epilogue    4 warps, one per tensor-memory lane quarter: drain the
+//   warps 10-13 epilogue, one per tensor-memory lane quarter: drain the
 //               accumulator (tcgen05.ld: a thread holds 32 consecutive weight
 //               rows of its token), dequantize, store fp16 y with 16-byte
 //               stores (or int32 accumulators), release the accumulator.
-//   converters  (not PRECONV) two groups of 4 warps taking alternate stages:
+//   converters  two groups of 4 warps (warps 2-9) taking alternate stages:
 //               each thread converts its weight row's 128 codes of the stage
 //               (two 64-K sub-tiles) and writes them in the canonical K-major
 //               swizzled layout, then reports to the even CTA's "ready"
 //               barrier.
-//   w-producer  (not PRECONV) TMA of the int8 codes [128 n][64 k] (INT4:
+//   warp 14     weight-code producer: TMA of the int8 codes [128 n][64 k] (INT4:
 //               packed [128 n][32 B]) into a separate 4-slot ring, one
 //               sub-tile per slot, running ahead of the conversion.
+//
+// Split-K: when the output tiles alone cannot occupy the GPU's CTA pairs (M
+// up to ~1000 tokens), each tile's K range is cut into ks slices processed by
+// different pairs.  A slice's accumulator is an exact integer (the per-tile
+// bound below holds for any part of K); it is stored as int32 into a
+// workspace [ks][M][N], and split_combine_kernel adds the ks partials in
+// int32 (exact) and applies the dequant.
 //
 // Exactness per tile: every partial sum of token m is bounded by
 // qmax_w * sum_k |q_a[m,k]| (qmax_w = 127 INT8, 8 INT4).  When that bound is
@@ -84,28 +88,28 @@ constexpr int kPSubBytes = kPHalf * kPSubK * 2;  // 16 KiB: one operand sub-tile
 constexpr int kPOpBytes = kPSub * kPSubBytes;    // 32 KiB: one operand of a stage
 constexpr int kPStageBytes = 2 * kPOpBytes;      // activations | weights
 constexpr int kP8Slots = 4;                      // int8 / int4 weight ring, one sub-tile per slot
+constexpr int kPStages = 3;
+constexpr int kPConvWarp0 = 2;                   // two groups of 4 converter warps
+constexpr int kPEpiWarp0 = 10;
+constexpr int kPW8Warp = 14;
+constexpr int kPThreads = 32 * (kPW8Warp + 1);
+// the even CTA's producer arrival (with both CTAs' activation bytes) + 4
+// converter warps x 2 CTAs
+constexpr int kPReadyCount = 9;
+constexpr uint32_t kPReadyBytes = 2 * kPOpBytes;
 constexpr uint64_t kPWaitNs = 2000000000ull;
 
-template <bool INT4, bool PRECONV>
+template <bool INT4>
 struct PCfg {
-  static constexpr int kStages = 3;
-  static constexpr int kConvWarp0 = 2;
-  static constexpr int kConvWarps = PRECONV ? 0 : 8;
-  static constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;
-  static constexpr int kW8Warp = kEpiWarp0 + 4;  // only without PRECONV
-  static constexpr int kThreads = 32 * (PRECONV ? kEpiWarp0 + 4 : kW8Warp + 1);
   static constexpr int kA8Bytes = INT4 ? kPHalf * kPSubK / 2 : kPHalf * kPSubK;
-  static constexpr int kA8Offset = kStages * kPStageBytes;
-  static constexpr int kBarOffset = kA8Offset + (PRECONV ? 0 : kP8Slots * 8192);
+  static constexpr int kA8Offset = kPStages * kPStageBytes;
+  static constexpr int kBarOffset = kA8Offset + kP8Slots * 8192;
   // ready, empty per stage; full8, empty8 per weight slot; accf x2, acce x2,
   // mma_done; then the tensor-memory slot and the abort flag
-  static constexpr int kBar8 = 2 * kStages;
+  static constexpr int kBar8 = 2 * kPStages;
   static constexpr int kBar2 = kBar8 + 2 * kP8Slots;
   static constexpr int kNumBars = kBar2 + 5;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;
-  // the even CTA's producer arrival (+ 4 converter warps x 2 CTAs)
-  static constexpr int kReadyCount = PRECONV ? 1 : 9;
-  static constexpr uint32_t kReadyBytes = (PRECONV ? 4 : 2) * kPOpBytes;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 static_assert(kPSubBytes % 1024 == 0, "sub-tiles must keep 1024-byte alignment for the swizzle");
@@ -113,6 +117,9 @@ static_assert(kPSubBytes % 1024 == 0, "sub-tiles must keep 1024-byte alignment f
 struct PairArgs {
   int M, N, K;
   int num_m_tiles, num_tiles;
+  int ks;          // K slices per tile (split-K when the tiles alone cannot fill the GPU)
+  int num_units;   // num_tiles * ks
+  int32_t* ws;     // ks > 1: partial accumulators [ks][M][N]
   const float* sa;
   const float* sw;
   __half* y;
@@ -150,12 +157,12 @@ __device__ __forceinline__ void store8_y(const PairArgs& p, int m, float sam, in
       make_uint4(h[0], h[1], h[2], h[3]);
 }
 
-template <bool INT4, int EPI, bool PRECONV>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PCfg<INT4, PRECONV>::kThreads, 1)
+template <bool INT4, int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const PairArgs p) {
-  using C = PCfg<INT4, PRECONV>;
-  constexpr int S = C::kStages;
+  using C = PCfg<INT4>;
+  constexpr int S = kPStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -184,14 +191,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PCfg<INT4, PRECONV>:
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(ready_bar(s), C::kReadyCount);
+      mbar_init(ready_bar(s), kPReadyCount);
       mbar_init(empty_bar(s), 1);
     }
-    if (!PRECONV) {
-      for (int j = 0; j < kP8Slots; ++j) {
-        mbar_init(full8_bar(j), 1);
-        mbar_init(empty8_bar(j), 4);   // the 4 warps of the converter group of this use
-      }
+    for (int j = 0; j < kP8Slots; ++j) {
+      mbar_init(full8_bar(j), 1);
+      mbar_init(empty8_bar(j), 4);     // the 4 warps of the converter group of this use
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -215,29 +220,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PCfg<INT4, PRECONV>:
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + C::kBarOffset + 8 * C::kNumBars);
   const int nkb = (p.K + kPBK - 1) / kPBK;
-  const int nch = (nkb + kPChunkKB - 1) / kPChunkKB;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint32_t ready_leader0 = mapa_shared(ready_bar(0), 0);
     int it = 0;
-    for (int tile = cid; tile < p.num_tiles; tile += nclusters) {
-      const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
+    for (int unit = cid; unit < p.num_units; unit += nclusters) {
+      const int tile = unit / p.ks, slice = unit % p.ks;
+      const int kb0 = slice * nkb / p.ks, kb1 = (slice + 1) * nkb / p.ks;
+      const int mt = tile % p.num_m_tiles;
       const int passes = pair_tile_fast(p, mt, lane) ? 1 : kPSlowPasses;
       if (lane == 0) {
         for (int pass = 0; pass < passes; ++pass)
-          for (int kb = 0; kb < nkb; ++kb, ++it) {
+          for (int kb = kb0; kb < kb1; ++kb, ++it) {
             const int s = it % S;
             const uint32_t ph = (it / S) & 1;
             if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, err, kPWaitNs)) break;
-            if (rank == 0) mbar_arrive_expect_tx(ready_bar(s), C::kReadyBytes);
+            if (rank == 0) mbar_arrive_expect_tx(ready_bar(s), kPReadyBytes);
             for (int t = 0; t < kPSub; ++t) {
               const int k0 = kb * kPBK + t * kPSubK;
               tma_load_2d_pair(sA(s) + t * kPSubBytes, &tmX, ready_leader0 + 8u * s, k0,
                                mt * kPTileM + rank * kPHalf);
-              if (PRECONV)
-                tma_load_2d_pair(sB(s) + t * kPSubBytes, &tmW, ready_leader0 + 8u * s, k0,
-                                 nt * kPTileN + rank * kPHalf);
             }
           }
       }
@@ -250,17 +253,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PCfg<INT4, PRECONV>:
       constexpr uint32_t idesc_fast = idesc_f16_f32(kPTileM, kPTileN);
       constexpr uint32_t idesc_slow = idesc_f16_f32(kPTileM, kPTileN / kPSlowPasses);
       int it = 0, ch = 0;
-      for (int tile = cid; tile < p.num_tiles; tile += nclusters) {
+      for (int unit = cid; unit < p.num_units; unit += nclusters) {
+        const int tile = unit / p.ks, slice = unit % p.ks;
+        const int kb0 = slice * nkb / p.ks, kb1 = (slice + 1) * nkb / p.ks;
         const int mt = tile % p.num_m_tiles;
         const bool fast = pair_tile_fast(p, mt, lane);
         if (lane == 0) {
           const int passes = fast ? 1 : kPSlowPasses;
           bool ok = true;
           for (int pass = 0; pass < passes && ok; ++pass) {
-            for (int kb = 0; kb < nkb; ++kb, ++it) {
-              const bool cstart = fast ? (kb == 0) : (kb % kPChunkKB) == 0;
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+              const int kr = kb - kb0;
+              const bool cstart = fast ? (kr == 0) : (kr % kPChunkKB) == 0;
               const bool cend =
-                  fast ? (kb == nkb - 1) : ((kb % kPChunkKB) == kPChunkKB - 1 || kb == nkb - 1);
+                  fast ? (kb == kb1 - 1) : ((kr % kPChunkKB) == kPChunkKB - 1 || kb == kb1 - 1);
               const int b = ch & 1;
               if (cstart && ch >= 2) {
                 // accumulator b was last used by chunk ch - 2: wait until both CTAs drained it
@@ -301,17 +307,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PCfg<INT4, PRECONV>:
       if (lane == 0) tc_commit_pair_mc(done_bar, 0x3);
       __syncwarp();
     }
-  } else if (!PRECONV && warp < C::kEpiWarp0) {
+  } else if (warp < kPEpiWarp0) {
     // ------------------------------------------------------------ converters
-    const int group = (warp - C::kConvWarp0) >> 2;   // takes the uses with it % 2 == group
+    const int group = (warp - kPConvWarp0) >> 2;   // takes the uses with it % 2 == group
     const int row = (warp & 3) * 32 + lane;
     const uint32_t ready_leader0 = mapa_shared(ready_bar(0), 0);
     int it = 0;
-    for (int tile = cid; tile < p.num_tiles; tile += nclusters) {
+    for (int unit = cid; unit < p.num_units; unit += nclusters) {
+      const int tile = unit / p.ks, slice = unit % p.ks;
+      const int kb0 = slice * nkb / p.ks, kb1 = (slice + 1) * nkb / p.ks;
       const int mt = tile % p.num_m_tiles;
       const int passes = pair_tile_fast(p, mt, lane) ? 1 : kPSlowPasses;
       for (int pass = 0; pass < passes; ++pass) {
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           if ((it & 1) != group) continue;
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
@@ -370,16 +378,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PCfg<INT4, PRECONV>:
         }
       }
     }
-  } else if (!PRECONV && warp == C::kW8Warp) {
+  } else if (warp == kPW8Warp) {
     // ------------------------------------------------------------ weight-code producer
     int it = 0;
-    for (int tile = cid; tile < p.num_tiles; tile += nclusters) {
+    for (int unit = cid; unit < p.num_units; unit += nclusters) {
+      const int tile = unit / p.ks, slice = unit % p.ks;
+      const int kb0 = slice * nkb / p.ks, kb1 = (slice + 1) * nkb / p.ks;
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
       const int passes = pair_tile_fast(p, mt, lane) ? 1 : kPSlowPasses;
       if (lane == 0) {
         bool ok = true;
         for (int pass = 0; pass < passes && ok; ++pass)
-          for (int kb = 0; kb < nkb && ok; ++kb)
+          for (int kb = kb0; kb < kb1 && ok; ++kb)
             for (int t = 0; t < kPSub; ++t, ++it) {
               const int j = it % kP8Slots;
               const uint32_t ph = (it / kP8Slots) & 1;
@@ -396,19 +406,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PCfg<INT4, PRECONV>:
       __syncwarp();
       if (*abort_flag) break;
     }
-  } else if (warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + 4) {
+  } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // tensor-memory lane quarter of this warp
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
+    const bool split = p.ks > 1;
     int ch = 0;
-    for (int tile = cid; tile < p.num_tiles; tile += nclusters) {
+    for (int unit = cid; unit < p.num_units; unit += nclusters) {
+      const int tile = unit / p.ks, slice = unit % p.ks;
+      const int kb0 = slice * nkb / p.ks, kb1 = (slice + 1) * nkb / p.ks;
+      const int nch = (kb1 - kb0 + kPChunkKB - 1) / kPChunkKB;
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
       const bool fast = pair_tile_fast(p, mt, lane);
       const int m = mt * kPTileM + static_cast<int>(rank) * kPHalf + q * 32 + lane;
       const bool mvalid = m < p.M;
       const float sam = (EPI == kEpiY && mvalid) ? __ldg(p.sa + m) : 0.0f;
       const int n_tile = nt * kPTileN;
+      int32_t* wrow = split ? p.ws + (static_cast<int64_t>(slice) * p.M + m) * p.N : nullptr;
+      // eight exact accumulator values of weight rows n0 .. n0 + 7: the
+      // result, or this slice's partial sums
+      auto emit8 = [&](int n0, const int (&iv)[8]) {
+        if (split) {
+          int4* d = reinterpret_cast<int4*>(wrow + n0);
+          d[0] = make_int4(iv[0], iv[1], iv[2], iv[3]);
+          d[1] = make_int4(iv[4], iv[5], iv[6], iv[7]);
+        } else if (EPI == kEpiAcc) {
+          const int64_t off = static_cast<int64_t>(m) * p.N + n0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) p.acc[off + i] = iv[i];
+        } else {
+          float f[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) f[i] = __int2float_rn(iv[i]);
+          store8_y(p, m, sam, n0, f);
+        }
+      };
       if (fast) {
         const int b = ch & 1;
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(accf_bar(b), (ch >> 1) & 1, abort_flag, err,
@@ -426,16 +459,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PCfg<INT4, PRECONV>:
             for (int g = 0; g < 4; ++g) {
               const int n0 = n_tile + c8 * 32 + g * 8;
               if (n0 < p.N) {   // N % 8 == 0: a group of 8 is all in or all out
-                if (EPI == kEpiAcc) {
-                  const int64_t off = static_cast<int64_t>(m) * p.N + n0;
+                int iv[8];
 #pragma unroll
-                  for (int i = 0; i < 8; ++i) p.acc[off + i] = __float2int_rn(__uint_as_float(v[g * 8 + i]));
-                } else {
-                  float f[8];
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v[g * 8 + i]);  // exact integers
-                  store8_y(p, m, sam, n0, f);
-                }
+                for (int i = 0; i < 8; ++i) iv[i] = __float2int_rn(__uint_as_float(v[g * 8 + i]));
+                emit8(n0, iv);
               }
             }
           }
@@ -473,16 +500,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PCfg<INT4, PRECONV>:
           for (int g = 0; g < 8; ++g) {
             const int n0 = n_tile + (g >> 2) * kPHalf + pass * 32 + (g & 3) * 8;
             if (n0 < p.N) {
-              if (EPI == kEpiAcc) {
-                const int64_t off = static_cast<int64_t>(m) * p.N + n0;
+              int iv[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) p.acc[off + i] = isum[g * 8 + i];
-              } else {
-                float f[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) f[i] = __int2float_rn(isum[g * 8 + i]);
-                store8_y(p, m, sam, n0, f);
-              }
+              for (int i = 0; i < 8; ++i) iv[i] = isum[g * 8 + i];
+              emit8(n0, iv);
             }
           }
         }
@@ -510,63 +531,70 @@ done:
   }
 }
 
-// int8 (or packed int4) weight codes [N, K] -> exact fp16 values [N, K]; one
-// thread per 16 consecutive values.
-template <bool INT4>
-__global__ void __launch_bounds__(256) convert_weights_kernel(const uint8_t* __restrict__ w,
-                                                              int64_t units, __half* __restrict__ out) {
-  for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < units;
-       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    uint32_t h[8];
-    if (!INT4) {
-      const uint4 v = ld_stream_v4(w + u * 16);
-      s8x4_to_h2x2(v.x, h[0], h[1]);
-      s8x4_to_h2x2(v.y, h[2], h[3]);
-      s8x4_to_h2x2(v.z, h[4], h[5]);
-      s8x4_to_h2x2(v.w, h[6], h[7]);
-    } else {
-      const uint2 v = __ldg(reinterpret_cast<const uint2*>(w + u * 8));
-      uint32_t t[4];
-      s4x8_to_h2x4(v.x, t);
-      h[0] = t[0];
-      h[1] = t[1];
-      h[2] = t[2];
-      h[3] = t[3];
-      s4x8_to_h2x4(v.y, t);
-      h[4] = t[0];
-      h[5] = t[1];
-      h[6] = t[2];
-      h[7] = t[3];
+// Split-K epilogue: y[m, n] (or acc) from the ks exact int32 partials of
+// ws [ks][M][N]; one thread per 8 consecutive outputs of a row.
+template <int EPI>
+__global__ void __launch_bounds__(256) split_combine_kernel(const int32_t* __restrict__ ws, int ks,
+                                                            int M, int N, const float* __restrict__ sa,
+                                                            const float* __restrict__ sw,
+                                                            __half* __restrict__ y,
+                                                            int32_t* __restrict__ acc) {
+  const int64_t groups = static_cast<int64_t>(M) * (N / 8);
+  const int64_t plane = static_cast<int64_t>(M) * N;
+  for (int64_t gi = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; gi < groups;
+       gi += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t off = gi * 8;
+    const int m = static_cast<int>(off / N);
+    const int n0 = static_cast<int>(off % N);
+    int iv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll 4
+    for (int sl = 0; sl < ks; ++sl) {
+      const int4* src = reinterpret_cast<const int4*>(ws + sl * plane + off);
+      const int4 a0 = __ldcs(src), a1 = __ldcs(src + 1);
+      iv[0] += a0.x; iv[1] += a0.y; iv[2] += a0.z; iv[3] += a0.w;
+      iv[4] += a1.x; iv[5] += a1.y; iv[6] += a1.z; iv[7] += a1.w;
     }
-    uint4* o = reinterpret_cast<uint4*>(out + u * 16);
-    o[0] = make_uint4(h[0], h[1], h[2], h[3]);
-    o[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    if (EPI == kEpiAcc) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[off + i] = iv[i];
+    } else {
+      const float sam = __ldg(sa + m);
+      uint32_t h[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half lo = __float2half_rn(
+            __fmul_rn(__fmul_rn(__int2float_rn(iv[2 * i]), sam), __ldg(sw + n0 + 2 * i)));
+        const __half hi = __float2half_rn(
+            __fmul_rn(__fmul_rn(__int2float_rn(iv[2 * i + 1]), sam), __ldg(sw + n0 + 2 * i + 1)));
+        h[i] = static_cast<uint32_t>(__half_as_ushort(lo)) |
+               (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+      }
+      *reinterpret_cast<uint4*>(y + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
   }
 }
 
-template <bool INT4, int EPI, bool PRECONV>
-cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmW, const PairArgs& a,
-                        cudaStream_t st) {
-  using C = PCfg<INT4, PRECONV>;
-  auto kern = gemm_pair_kernel<INT4, EPI, PRECONV>;
-  static std::atomic<uint64_t> attr_done{0};
-  cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::kSmemBytes,
-                                          attr_done);
-  if (e != cudaSuccess) return e;
-  // clusters that fit on the GPU at once (one CTA per SM), cached per device
-  static std::atomic<int> max_clusters[64];
+// CTA pairs that fit on the current device at once (one CTA per SM), cached
+// per device.  All instantiations use the same shared memory and threads.
+cudaError_t pair_max_clusters(int* out) {
+  static std::atomic<int> cached[64];
   int dev = 0;
-  e = cudaGetDevice(&dev);
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int nc = dev < 64 ? max_clusters[dev].load(std::memory_order_relaxed) : 0;
+  int nc = dev < 64 ? cached[dev].load(std::memory_order_relaxed) : 0;
   if (nc <= 0) {
+    auto kern = gemm_pair_kernel<false, kEpiY>;
+    static std::atomic<uint64_t> attr_done{0};
+    e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), PCfg<false>::kSmemBytes,
+                                attr_done);
+    if (e != cudaSuccess) return e;
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
-    cfg.blockDim = dim3(C::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.blockDim = dim3(kPThreads, 1, 1);
+    cfg.dynamicSmemBytes = PCfg<false>::kSmemBytes;
     int q = 0;
     if (cudaOccupancyMaxActiveClusters(&q, reinterpret_cast<const void*>(kern), &cfg) !=
             cudaSuccess ||
@@ -575,74 +603,108 @@ cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmW, const Pa
       q = sms / 2;
     }
     nc = q;
-    if (dev < 64) max_clusters[dev].store(nc, std::memory_order_relaxed);
+    if (dev < 64) cached[dev].store(nc, std::memory_order_relaxed);
   }
-  const int clusters = a.num_tiles < nc ? a.num_tiles : nc;
-  kern<<<2 * clusters, C::kThreads, C::kSmemBytes, st>>>(tmX, tmW, a);
-  return cudaGetLastError();
+  *out = nc;
+  return cudaSuccess;
 }
 
+// K slices per tile: 1 when the tiles fill the pairs; otherwise the split
+// that minimises (rounds of units over the pairs) x (stages per slice) plus
+// the cost of the partial sums (written, read back and combined), keeping at
+// least two 128-K stages per slice and at most 8 slices.
+int pair_split(int64_t M, int64_t N, int64_t K, int nc) {
+  const int64_t tiles = ((M + kPTileM - 1) / kPTileM) * ((N + kPTileN - 1) / kPTileN);
+  const int64_t nkb = (K + kPBK - 1) / kPBK;
+  if (tiles >= nc || nkb < 4) return 1;
+  // in units of one pipeline stage of one pair (~0.5 us): a combine launch
+  // costs ~6 stages, each tile-slice of partials ~0.25 stage of traffic
+  int best = 1;
+  double best_cost = static_cast<double>(nkb);
+  for (int ks = 2; ks <= 8 && ks <= nkb / 2; ++ks) {
+    const int64_t rounds = (tiles * ks + nc - 1) / nc;
+    const double cost = static_cast<double>(rounds * ((nkb + ks - 1) / ks)) + 6.0 +
+                        0.25 * static_cast<double>(tiles * ks) * static_cast<double>(M < kPTileM ? M : kPTileM) / kPTileM;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = ks;
+    }
+  }
+  return best;
+}
+
+size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+
 template <bool INT4, int EPI>
-cudaError_t launch_pair_any(const CUtensorMap& tmX, const CUtensorMap& tmW, const PairArgs& a,
-                            bool preconv, cudaStream_t st) {
-  return preconv ? launch_pair<INT4, EPI, true>(tmX, tmW, a, st)
-                 : launch_pair<INT4, EPI, false>(tmX, tmW, a, st);
+cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmW, const PairArgs& a,
+                        int nc, cudaStream_t st) {
+  using C = PCfg<INT4>;
+  auto kern = gemm_pair_kernel<INT4, EPI>;
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::kSmemBytes,
+                                          attr_done);
+  if (e != cudaSuccess) return e;
+  const int clusters = a.num_units < nc ? a.num_units : nc;
+  kern<<<2 * clusters, kPThreads, C::kSmemBytes, st>>>(tmX, tmW, a);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_convert_weights(const uint8_t* w, int64_t N, int64_t K, bool int4, __half* out,
-                                   int num_sms, cudaStream_t st) {
-  const int64_t units = N * K / 16;
-  int64_t blocks = (units + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  if (int4)
-    convert_weights_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, st>>>(w, units, out);
-  else
-    convert_weights_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(w, units, out);
-  return cudaGetLastError();
+size_t gemm_pair_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  int nc = 0;
+  if (pair_max_clusters(&nc) != cudaSuccess) return 0;
+  const int ks = pair_split(M, N, K, nc);
+  if (ks <= 1) return 0;
+  return round256(static_cast<size_t>(ks) * M * N * 4);
 }
 
 cudaError_t launch_gemm_pair(const __half* qa16, const float* sa, const int* row_l1, int64_t M,
-                             int64_t N, int64_t K, const uint8_t* w, bool int4, const __half* w16,
-                             const float* sw, int mode, __half* y, int32_t* acc, cudaStream_t st) {
+                             int64_t N, int64_t K, const uint8_t* w, bool int4, const float* sw,
+                             int mode, __half* y, int32_t* acc, void* workspace, cudaStream_t st) {
   CUtensorMap tmX, tmW;
   if (!make_tensor_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qa16, K, M, K * 2, kPSubK, kPHalf,
                           CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  const bool preconv = w16 != nullptr;
-  if (preconv) {
-    if (!make_tensor_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, w16, K, N, K * 2, kPSubK, kPHalf,
-                            CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-  } else {
-    const uint64_t wbytes = int4 ? K / 2 : K;
-    if (!make_tensor_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, wbytes, N, wbytes,
-                            int4 ? kPSubK / 2 : kPSubK, kPHalf,
-                            int4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B))
-      return cudaErrorInvalidValue;
-  }
+  const uint64_t wbytes = int4 ? K / 2 : K;
+  if (!make_tensor_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, wbytes, N, wbytes,
+                          int4 ? kPSubK / 2 : kPSubK, kPHalf,
+                          int4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
   PairArgs a;
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
   a.num_m_tiles = static_cast<int>((M + kPTileM - 1) / kPTileM);
   a.num_tiles = a.num_m_tiles * static_cast<int>((N + kPTileN - 1) / kPTileN);
+  int nc = 0;
+  cudaError_t e = pair_max_clusters(&nc);
+  if (e != cudaSuccess) return e;
+  a.ks = workspace ? pair_split(M, N, K, nc) : 1;
+  a.num_units = a.num_tiles * a.ks;
+  a.ws = a.ks > 1 ? static_cast<int32_t*>(workspace) : nullptr;
   a.sa = sa;
   a.sw = sw;
   a.y = y;
   a.acc = acc;
   a.row_l1 = row_l1;
   a.l1_limit = (1 << 23) / (int4 ? 8 : 127);
-  cudaError_t e = device_error_word(&a.err);
+  e = device_error_word(&a.err);
   if (e != cudaSuccess) return e;
   if (int4)
-    return mode == kEpiY ? launch_pair_any<true, kEpiY>(tmX, tmW, a, preconv, st)
-                         : launch_pair_any<true, kEpiAcc>(tmX, tmW, a, preconv, st);
-  return mode == kEpiY ? launch_pair_any<false, kEpiY>(tmX, tmW, a, preconv, st)
-                       : launch_pair_any<false, kEpiAcc>(tmX, tmW, a, preconv, st);
+    e = mode == kEpiY ? launch_pair<true, kEpiY>(tmX, tmW, a, nc, st)
+                      : launch_pair<true, kEpiAcc>(tmX, tmW, a, nc, st);
+  else
+    e = mode == kEpiY ? launch_pair<false, kEpiY>(tmX, tmW, a, nc, st)
+                      : launch_pair<false, kEpiAcc>(tmX, tmW, a, nc, st);
+  if (e != cudaSuccess || a.ks == 1) return e;
+  const int64_t groups = M * (N / 8);
+  const int blocks = static_cast<int>((groups + 255) / 256 < 4096 ? (groups + 255) / 256 : 4096);
+  if (mode == kEpiY)
+    split_combine_kernel<kEpiY><<<blocks, 256, 0, st>>>(a.ws, a.ks, a.M, a.N, sa, sw, y, acc);
+  else
+    split_combine_kernel<kEpiAcc><<<blocks, 256, 0, st>>>(a.ws, a.ks, a.M, a.N, sa, sw, y, acc);
+  return cudaGetLastError();
 }
 
 }  // namespace cider

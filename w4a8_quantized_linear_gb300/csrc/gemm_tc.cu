@@ -392,11 +392,11 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
 }  // namespace
 
 cudaError_t launch_gemm_tc(const __half* qa16, const float* sa, const int* row_l1, int64_t M,
-                           int64_t N, int64_t K, const uint8_t* w, bool int4, const __half* w16,
-                           const float* sw, int group_size, int mode, __half* y, int32_t* acc,
+                           int64_t N, int64_t K, const uint8_t* w, bool int4, const float* sw,
+                           int group_size, int mode, __half* y, int32_t* acc, void* workspace,
                            int num_sms, cudaStream_t st) {
   if (group_size == 0)
-    return launch_gemm_pair(qa16, sa, row_l1, M, N, K, w, int4, w16, sw, mode, y, acc, st);
+    return launch_gemm_pair(qa16, sa, row_l1, M, N, K, w, int4, sw, mode, y, acc, workspace, st);
   CUtensorMap tmA, tmB;
   if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qa16, K, M, K * 2, kBK, kTileM,
                    CU_TENSOR_MAP_SWIZZLE_128B))
@@ -423,6 +423,10 @@ cudaError_t launch_gemm_tc(const __half* qa16, const float* sa, const int* row_l
                          : launch_tc<true, true, kEpiAcc>(tmA, tmB, a, num_sms, st);
   return mode == kEpiY ? launch_tc<false, true, kEpiY>(tmA, tmB, a, num_sms, st)
                        : launch_tc<false, true, kEpiAcc>(tmA, tmB, a, num_sms, st);
+}
+
+size_t gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size) {
+  return group_size == 0 ? gemm_pair_workspace_bytes(M, N, K) : 0;
 }
 
 cudaError_t device_error_word(int** ptr) {

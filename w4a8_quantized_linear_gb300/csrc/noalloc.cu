@@ -127,8 +127,8 @@ extern "C" cider_status_t cider_w8a8_linear_noalloc(const void* x, int64_t M, in
       int* row_l1 = reinterpret_cast<int*>(base + qbytes + vbytes);
       e = cider::launch_quant_act_f16(static_cast<const __half*>(x), M, K, q16, sa, row_l1, st);
       if (e == cudaSuccess)
-        e = cider::launch_gemm_tc(q16, sa, row_l1, M, N, K, w, false, nullptr, sw, group_size,
-                                  cider::kEpiY, yh, nullptr, sms, st);
+        e = cider::launch_gemm_tc(q16, sa, row_l1, M, N, K, w, false, sw, group_size, cider::kEpiY,
+                                  yh, nullptr, /*workspace: never split*/ nullptr, sms, st);
     }
     if (e != cudaSuccess) {
       cudaGetLastError();
