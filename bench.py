@@ -186,20 +186,20 @@ def library_path(M: int, K: int, gs: int):
     """(dominant kernel, kernel launches per step) of the library's dispatch for
     one linear call: the same limits as gemv_fits() and launch_gemm_tc() in the
     CUDA sources (small-M GEMV up to M=16 when its activation block and a ring
-    of at least four 4 KiB weight tiles fit in shared memory; otherwise the
-    per-token quantization kernel, for per-channel problems with M >= 8192 a
-    weight conversion pass, and one tensor-core GEMM)."""
+    of at least four 4 KiB weight tiles fit in shared memory, preceded by the
+    per-token quantization kernel from M=4; otherwise the quantization kernel
+    followed by one tensor-core GEMM)."""
     if 1 <= M <= 16:
         mb = 1
         while mb < M:
             mb *= 2
         if mb * K <= 200 * 1024 and (227 * 1024 - 4096 - mb * K) // 4096 >= 4:
-            return "gemv_kernel (small-M weight-streaming GEMV, fused quantization)", 1
+            if M <= 3:   # kGemvFusedMaxM: the GEMV quantizes the rows itself
+                return "gemv_kernel (small-M weight-streaming GEMV, fused quantization)", 1
+            return "gemv_kernel (small-M weight-streaming GEMV, tensor-core form)", 2
     if gs:
         return "gemm_tc_kernel (tcgen05 kind::f16 on exact integer codes, per-group epilogue)", 2
-    if M >= 8192:   # kPreconvMinM: weights converted to fp16 once per call
-        return ("gemm_pair_kernel (tcgen05 cta_group::2, 256x256 tiles, fp16 weights by TMA)", 3)
-    return "gemm_pair_kernel (tcgen05 cta_group::2, 256x256 tiles, in-kernel conversion)", 2
+    return "gemm_pair_kernel (tcgen05 cta_group::2 on CTA pairs, 256x256 tiles)", 2
 
 
 def ncu_traffic(workload: str):
@@ -336,19 +336,27 @@ def run_ours(a):
     torch.cuda.synchronize()
 
     use_graph = a.graph == "on" or (a.graph == "auto" and a.M <= 16)
-    graph = None
+    graph = graph_timed = None
     per_graph = 1
     if use_graph:
-        # one graph holds `per_graph` consecutive steps (a divisor of K), replayed K / per_graph times
+        # one graph holds `per_graph` consecutive steps (a divisor of K), replayed K / per_graph
+        # times in the timed region.  A second graph of the same steps with the library's kernel
+        # timing events as nodes is replayed as often right after it, for the kernel durations:
+        # the event nodes add gaps between the launches, so they stay out of the timed steps.
         per_graph = max(d for d in range(1, min(a.steps, 64) + 1) if a.steps % d == 0)
-        cider.cider_timing_begin(per_graph)    # the kernel-timing events become graph nodes
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
+            for i in range(per_graph):
+                step(i)
+        cider.cider_timing_begin(per_graph)    # the kernel-timing events become graph nodes
+        graph_timed = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_timed):
             for i in range(per_graph):
                 step(i)
         torch.cuda.synchronize()
         for _ in range(3):
             graph.replay()
+            graph_timed.replay()
         torch.cuda.synchronize()
     else:
         cider.cider_timing_begin(a.steps)   # events are created here, outside the timed region
@@ -371,9 +379,15 @@ def run_ours(a):
             step(i)
     stop.record()
     torch.cuda.synchronize()
+    if graph_timed is not None:
+        # kernel durations: the same steps, replayed with the timing events
+        for _ in range(a.steps // per_graph):
+            graph_timed.replay()
+        torch.cuda.synchronize()
     if clocks:
         clocks.mark(False)
     n_timed, gemm_total_ms = cider.cider_timing_end()
+    del graph_timed
     if ws > 1:
         torch.distributed.barrier()
     clk = clocks.stop() if clocks else None
@@ -422,17 +436,22 @@ def run_ours(a):
 
     peaks, peak_src = measured_peaks()
     kernel_name, launches_per_step = library_path(a.M, a.K, a.gs)
-    small_m = launches_per_step == 1
+    small_m = kernel_name.startswith("gemv")
     wl = workload_name(a)
     if small_m:
         wbytes = a.N * a.K if a.bits == 8 else a.N * a.K // 2
         G = a.K // a.gs if a.gs else 1
-        # the fused kernel reads x (fp16), the weight codes and scales, writes y
+        # algorithmic bytes of the step: weight codes and scales, x (fp16), y.  The step is
+        # timed as CUDA-graph replays; its duration bounds the kernels' from above, so
+        # achieved = bytes / step time is a lower bound.  (Timing events placed as graph
+        # nodes around a ~10 us kernel add several us of gaps to what they measure.)
         alg_bytes = wbytes + 4 * a.N * G + 2 * a.M * a.K + 2 * a.M * a.N
-        achieved = alg_bytes / gemm_avg_s / 1e9
+        achieved = alg_bytes / (el_ms / a.steps * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(wl),
-                "kernel": kernel_name,
+                "kernel": kernel_name + ("" if launches_per_step == 1 else
+                                         " with the quantization kernel (whole step)"),
+                "timing": "whole step per CUDA-graph replay (upper bound of the kernel time)",
                 "peak_source": f"{peak_src} hbm_gbs",
                 "algorithmic_bytes_per_launch": alg_bytes}
     else:
@@ -458,7 +477,8 @@ def run_ours(a):
                    "l2": f"inputs larger than L2: {n_sets} rotating x/qw/y sets "
                          f"({n_sets * set_bytes / 1e6:.0f} MB)",
                    "gemm_ms_avg": gemm_avg_s * 1e3,
-                   "launch": (f"CUDA graph of {per_graph} steps, replayed {a.steps // per_graph} times"
+                   "launch": (f"CUDA graph of {per_graph} steps, replayed {a.steps // per_graph} times; "
+                              "kernel durations from a second replay pass with timing events"
                               if graph is not None else "direct launches from Python")},
         "roofline": roof,
         "gpu_launches": launches_per_step * a.steps,

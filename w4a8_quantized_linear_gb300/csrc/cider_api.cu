@@ -220,10 +220,27 @@ cider_status_t run_linear(const LinearArgs& a) {
   const int gs = a.group_size;
   Scratch scratch;
   if (cider::gemv_fits(a.M, a.K)) {
-    // small M: one kernel, quantizing the activation rows itself when given x
+    // small M.  Up to 3 tokens the GEMV quantizes the rows itself (every CTA
+    // repeats that work, which is cheaper than a second launch for so few
+    // rows); from 4 tokens one quantization kernel writes the int8 codes first.
+    const __half* xg = static_cast<const __half*>(a.x);
+    const int8_t* qa = a.qa;
+    const float* sa = a.sa;
+    if (xg && a.M >= cider::kGemvFusedMaxM + 1) {
+      const size_t qbytes = round_up(static_cast<size_t>(a.M * a.K), 256);
+      cudaError_t e = scratch_alloc(scratch, dev, qbytes + round_up(4 * a.M, 256), a.st);
+      if (e != cudaSuccess) return cuda_status(e);
+      int8_t* qs = static_cast<int8_t*>(scratch.ptr);
+      float* ss = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch.ptr) + qbytes);
+      e = cider::launch_quant_act_s8(xg, a.M, a.K, qs, ss, a.st);
+      if (e != cudaSuccess) return cuda_status(e);
+      xg = nullptr;
+      qa = qs;
+      sa = ss;
+    }
     return cuda_status(timed_launch(a.st, [&] {
-      return cider::launch_gemv(static_cast<const __half*>(a.x), a.qa, a.sa, a.M, a.N, a.K, w,
-                                a.int4, a.sw, gs, a.mode, y, a.acc, sms, a.st);
+      return cider::launch_gemv(xg, qa, sa, a.M, a.N, a.K, w, a.int4, a.sw, gs, a.mode, y, a.acc,
+                                sms, a.st);
     }));
   }
   // tensor-core path: activation codes as fp16 integers, scales, row sums of |code|

@@ -16,6 +16,17 @@
 // N is too small to fill the GPU with whole rows; partial sums then meet in
 // shared memory.  Grids are sized to be resident in one wave.
 //
+// For 4 to 16 tokens the dot products run on the tensor
+// cores instead (mma.sync m16n8k16, fp16 operands holding the exact codes,
+// fp32 accumulation drained to int32 after every 64 codes, so every partial
+// sum stays below 2^20 and exact; INT4 codes are unpacked to int8 first):
+// each tile is split into four 64-byte quarters, one per warp, and the two
+// sets of four warps take alternate
+// tiles; the warps' partial sums meet in shared memory at the end of each
+// 16-row block.  With dp4a at these M each weight byte costs M / 4
+// instructions plus shared-memory reloads of the activations, which made the
+// kernel compute-bound well below the weight bandwidth.
+//
 // Accumulation is exact int32 (dp4a).  Per channel: the lane sums are reduced
 // exactly and y = fp16((float(acc) * s_a) * s_w).  Per group: every chunk
 // lies inside one group; the lane's exact partial of that group is scaled by
@@ -43,6 +54,17 @@ constexpr int kTileBytes = kBoxRows * kBoxBytes;     // 4 KiB
 constexpr int kRingMax = 8;
 constexpr int kStageBatch = 4;    // 16-byte activation loads in flight per thread while staging
 constexpr int kSmemBudget = 227 * 1024 - 4096;       // dynamic: leave room for static arrays
+constexpr int kRedBytes = kGemvWarps * 32 * 8 * 4;   // tensor-core form: block reduction buffer
+
+// 16 x 8 x 16 tensor-core product on fp16 fragments, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
 // Eight codes (byte i = code i) in natural order, or for INT4 weights in the
 // order [codes 0,2,4,6 | codes 1,3,5,7] that lines up with the low / high
@@ -73,9 +95,10 @@ struct GemvArgs {
 // block; lane l works on row 2w + l/16 and on its 16-byte chunk l%16 of each
 // tile, accumulating over the tiles of the block, and the 16 lanes of a row
 // are reduced at the block's end.
-template <int MB, bool INT4, bool PG, int EPI, bool FUSEQ>
+template <int MB, bool INT4, bool PG, int EPI, bool FUSEQ, bool MMA>
 __global__ void __launch_bounds__(kGemvThreads, 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tmW, const GemvArgs p) {
+  static_assert(!MMA || (MB >= 4 && !(PG && EPI == kEpiAcc)), "tensor-core form");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1 KiB aligned
   uint8_t* ring = smem;
@@ -100,7 +123,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     s_abort = 0u;
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&s_full[i]), 1);
-      mbar_init(smem_u32(&s_empty[i]), kGemvWarps);
+      mbar_init(smem_u32(&s_empty[i]), MMA ? kGemvWarps / 2 : kGemvWarps);
     }
     fence_mbar_init();
   }
@@ -209,6 +232,149 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   }
   named_barrier_sync(1, cthreads);
 
+  if constexpr (MMA) {
+    // ---------------------------------------------------- tensor-core form
+    __shared__ int s_red[kGemvWarps][32 * 8];
+    const int q = warp & 3;         // 64-code quarter of every tile
+    const int par = warp >> 2;      // takes the tiles with it % 2 == par
+    const int g8 = lane >> 2, t4 = lane & 3;
+    // fragment k order: in k-step j, thread t4 holds codes 16 t4 + 4 j .. + 3
+    // of its quarter for both operands (the same permutation of K for A and B)
+    const uint8_t* arow0 = s_act + static_cast<size_t>(g8) * K;
+    const uint8_t* arow1 = s_act + static_cast<size_t>(g8 + 8) * K;
+    int it = 0;
+    for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
+      int iacc[8];    // [n-block][4]: tokens g8 (0, 1) / g8 + 8 (2, 3), rows 2 t4 (+1)
+      float facc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        iacc[i] = 0;
+        facc[i] = 0.0f;
+      }
+      for (int kt = 0; kt < ntk; ++kt, ++it) {
+        if ((it & 1) != par) continue;
+        const int s = it % NS;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&s_full[s]), (it / NS) & 1,
+                                                       &s_abort, p.err, kKernelWaitTimeoutNs)))
+          return;
+        const uint8_t* wt = ring + s * kTileBytes + q * 64;   // the quarter: 64 bytes per row
+        // scale the exact partial sums of one group (per group) or add them (per channel)
+        auto drain = [&](float (&c0)[4], float (&c1)[4], int gi) {
+          if (!PG) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              iacc[i] += __float2int_rn(c0[i]);   // exact integers below 2^20
+              iacc[4 + i] += __float2int_rn(c1[i]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int64_t n = b * kBoxRows + (i >> 2) * 8 + 2 * t4 + (i & 1);
+              const int m = g8 + 8 * ((i >> 1) & 1);
+              if (n < N && m < MB) {
+                const float sc = __fmul_rn(s_sa[m], __ldg(p.sw + n * p.G + gi));
+                facc[i] = fmaf(sc, i < 4 ? c0[i] : c1[i - 4], facc[i]);
+              }
+            }
+          }
+        };
+        if (!INT4) {
+          // thread t4 holds codes 16 t4 .. + 15 of the quarter; k-step j uses its word j
+          const int k0 = kt * kBoxBytes + q * 64 + 16 * t4;
+          uint4 al = make_uint4(0u, 0u, 0u, 0u), ah = al;
+          if (k0 < K && g8 < MB) al = *reinterpret_cast<const uint4*>(arow0 + k0);
+          if (k0 < K && MB == 16) ah = *reinterpret_cast<const uint4*>(arow1 + k0);
+          const uint4 w0 = *reinterpret_cast<const uint4*>(wt + g8 * kBoxBytes + 16 * t4);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(wt + (8 + g8) * kBoxBytes + 16 * t4);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&s_empty[s]));  // the tile is in registers now
+          const uint32_t av[4] = {al.x, al.y, al.z, al.w}, hv[4] = {ah.x, ah.y, ah.z, ah.w};
+          const uint32_t bv0[4] = {w0.x, w0.y, w0.z, w0.w}, bv1[4] = {w1.x, w1.y, w1.z, w1.w};
+          float c0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t a0, a2, a1 = 0u, a3 = 0u, x0, x1, y0, y1;
+            s8x4_to_h2x2(av[j], a0, a2);
+            if (MB == 16) s8x4_to_h2x2(hv[j], a1, a3);
+            s8x4_to_h2x2(bv0[j], x0, x1);
+            s8x4_to_h2x2(bv1[j], y0, y1);
+            mma_16816(c0, a0, a1, a2, a3, x0, x1);
+            mma_16816(c1, a0, a1, a2, a3, y0, y1);
+          }
+          drain(c0, c1, PG ? (kt * kBoxBytes + q * 64) / p.gs : 0);
+        } else {
+          // the quarter holds 128 codes in two 64-code halves; thread t4 holds codes
+          // 16 t4 .. + 15 of each half (8 packed bytes), so every k-step stays inside
+          // one half (one group when gs = 64).  Staged activations are in the packed
+          // order [even codes | odd codes] of every 8, matching the nibbles.
+          const int cb = kt * (2 * kBoxBytes) + q * 128;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int k0 = cb + 64 * h + 16 * t4;
+            uint4 al = make_uint4(0u, 0u, 0u, 0u), ah = al;
+            if (k0 < K && g8 < MB) al = *reinterpret_cast<const uint4*>(arow0 + k0);
+            if (k0 < K && MB == 16) ah = *reinterpret_cast<const uint4*>(arow1 + k0);
+            const uint2 w0 = *reinterpret_cast<const uint2*>(wt + g8 * kBoxBytes + 32 * h + 8 * t4);
+            const uint2 w1 = *reinterpret_cast<const uint2*>(wt + (8 + g8) * kBoxBytes + 32 * h + 8 * t4);
+            if (h == 1) {
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&s_empty[s]));  // the tile is in registers now
+            }
+            const uint32_t av[4] = {al.x, al.y, al.z, al.w}, hv[4] = {ah.x, ah.y, ah.z, ah.w};
+            const uint32_t wv0[2] = {w0.x, w0.y}, wv1[2] = {w1.x, w1.y};
+            float c0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {          // packed word j: codes 8 j .. 8 j + 7
+              const uint32_t u0 = wv0[j] ^ 0x88888888u, u1 = wv1[j] ^ 0x88888888u;
+              const uint32_t e0 = offset_nibbles_to_s8x4(u0 & 0x0F0F0F0Fu);
+              const uint32_t o0 = offset_nibbles_to_s8x4((u0 >> 4) & 0x0F0F0F0Fu);
+              const uint32_t e1 = offset_nibbles_to_s8x4(u1 & 0x0F0F0F0Fu);
+              const uint32_t o1 = offset_nibbles_to_s8x4((u1 >> 4) & 0x0F0F0F0Fu);
+#pragma unroll
+              for (int oe = 0; oe < 2; ++oe) {     // even codes, then odd codes
+                uint32_t a0, a2, a1 = 0u, a3 = 0u, x0, x1, y0, y1;
+                s8x4_to_h2x2(av[2 * j + oe], a0, a2);
+                if (MB == 16) s8x4_to_h2x2(hv[2 * j + oe], a1, a3);
+                s8x4_to_h2x2(oe ? o0 : e0, x0, x1);
+                s8x4_to_h2x2(oe ? o1 : e1, y0, y1);
+                mma_16816(c0, a0, a1, a2, a3, x0, x1);
+                mma_16816(c1, a0, a1, a2, a3, y0, y1);
+              }
+            }
+            drain(c0, c1, PG ? (cb + 64 * h) / p.gs : 0);
+          }
+        }
+      }
+      // the 8 warps' partials of the block's 16 tokens x 16 rows meet in shared memory
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s_red[warp][lane * 8 + i] = PG ? __float_as_int(facc[i]) : iacc[i];
+      named_barrier_sync(1, cthreads);
+      {
+        const int m = ctid >> 4, nl = ctid & 15;   // one output per consumer thread
+        const int src = ((m & 7) * 4 + ((nl & 7) >> 1)) * 8 + (nl >> 3) * 4 + (m >> 3) * 2 + (nl & 1);
+        const int64_t n = b * kBoxRows + nl;
+        if (m < M && n < N) {
+          const int64_t off = static_cast<int64_t>(m) * N + n;
+          if (!PG) {
+            int v = 0;
+#pragma unroll
+            for (int w = 0; w < kGemvWarps; ++w) v += s_red[w][src];
+            if (EPI == kEpiAcc)
+              p.acc[off] = v;
+            else
+              p.y[off] = __float2half_rn(__fmul_rn(__fmul_rn(__int2float_rn(v), s_sa[m]), __ldg(p.sw + n)));
+          } else {
+            float v = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kGemvWarps; ++w) v += __int_as_float(s_red[w][src]);
+            p.y[off] = __float2half_rn(v);
+          }
+        }
+      }
+      named_barrier_sync(1, cthreads);   // s_red is rewritten by the next block
+    }
+  } else {
+  // ---------------------------------------------------- dp4a form
   const int rl = 2 * warp + (lane >> 4);  // row within the block
   const int ch = lane & 15;               // 16-byte chunk within the tile row
   int it = 0;
@@ -310,26 +476,27 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       }
     }
   }
+}  // dp4a form
 }
 
-int ring_slots(int64_t MB, int64_t K) {
-  const int64_t room = kSmemBudget - MB * K;
+int ring_slots(int64_t MB, int64_t K, bool mma = false) {
+  const int64_t room = kSmemBudget - (mma ? kRedBytes : 0) - MB * K;
   int64_t ns = room / kTileBytes;
   if (ns > kRingMax) ns = kRingMax;
   return static_cast<int>(ns);
 }
 
-template <int MB, bool INT4, bool PG, int EPI, bool FUSEQ>
+template <int MB, bool INT4, bool PG, int EPI, bool FUSEQ, bool MMA>
 cudaError_t launch_one(const __half* x, const int8_t* qa, const float* sa, int64_t M, int64_t N,
                        int64_t K, const uint8_t* w, const float* sw, int gs, __half* y,
                        int32_t* acc, int num_sms, cudaStream_t st) {
-  auto kern = gemv_kernel<MB, INT4, PG, EPI, FUSEQ>;
-  const int NS = ring_slots(MB, K);
+  auto kern = gemv_kernel<MB, INT4, PG, EPI, FUSEQ, MMA>;
+  const int NS = ring_slots(MB, K, MMA);
   if (NS < 4) return cudaErrorInvalidValue;
   const size_t smem = static_cast<size_t>(NS) * kTileBytes + static_cast<size_t>(MB) * K + 1024;
   static std::atomic<uint64_t> attr_done{0};
-  cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), kSmemBudget + 1024,
-                                          attr_done);
+  cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern),
+                                          kSmemBudget - (MMA ? kRedBytes : 0) + 1024, attr_done);
   if (e != cudaSuccess) return e;
   CUtensorMap tmW;
   const uint64_t rowbytes = static_cast<uint64_t>(INT4 ? K / 2 : K);
@@ -362,7 +529,7 @@ cudaError_t launch_one(const __half* x, const int8_t* qa, const float* sa, int64
     regs = fa.numRegs > 0 ? fa.numRegs : 128;
     regs_cache.store(regs, std::memory_order_relaxed);
   }
-  int occ = static_cast<int>((228 * 1024) / (smem + 2 * 1024));
+  int occ = static_cast<int>((228 * 1024) / (smem + (MMA ? kRedBytes : 0) + 2 * 1024));
   const int by_regs = 65536 / (((regs + 7) / 8) * 8 * kGemvThreads);
   if (by_regs < occ) occ = by_regs;
   if (occ > 2048 / kGemvThreads) occ = 2048 / kGemvThreads;
@@ -381,9 +548,28 @@ cudaError_t dispatch_mb(const __half* x, const int8_t* qa, const float* sa, int6
                         __half* y, int32_t* acc, int num_sms, cudaStream_t st) {
   const bool pg = gs > 0;
   const bool fq = x != nullptr;
+  // tensor-core form for 4..16 tokens with int8 weights (not for the exact
+  // per-group accumulators, which keep the dp4a lanes' group reductions)
+  constexpr bool kMmaMB = MB >= 4;
+  if (kMmaMB && !(pg && mode == kEpiAcc) && ring_slots(MB, K, true) >= 4) {
+#define CIDER_GEMV_MMA_CASE(I4, P, E, F)                                                      \
+  if (int4 == I4 && pg == P && mode == E && fq == F)                                          \
+    return launch_one<MB, I4, P, E, F, kMmaMB>(x, qa, sa, M, N, K, w, sw, gs, y, acc, num_sms, st);
+    CIDER_GEMV_MMA_CASE(false, false, kEpiY, true)
+    CIDER_GEMV_MMA_CASE(false, true, kEpiY, true)
+    CIDER_GEMV_MMA_CASE(false, false, kEpiY, false)
+    CIDER_GEMV_MMA_CASE(false, true, kEpiY, false)
+    CIDER_GEMV_MMA_CASE(false, false, kEpiAcc, false)
+    CIDER_GEMV_MMA_CASE(true, false, kEpiY, true)
+    CIDER_GEMV_MMA_CASE(true, true, kEpiY, true)
+    CIDER_GEMV_MMA_CASE(true, false, kEpiY, false)
+    CIDER_GEMV_MMA_CASE(true, true, kEpiY, false)
+    CIDER_GEMV_MMA_CASE(true, false, kEpiAcc, false)
+#undef CIDER_GEMV_MMA_CASE
+  }
 #define CIDER_GEMV_CASE(I4, P, E, F)                                                          \
   if (int4 == I4 && pg == P && mode == E && fq == F)                                          \
-    return launch_one<MB, I4, P, E, F>(x, qa, sa, M, N, K, w, sw, gs, y, acc, num_sms, st);
+    return launch_one<MB, I4, P, E, F, false>(x, qa, sa, M, N, K, w, sw, gs, y, acc, num_sms, st);
   CIDER_GEMV_CASE(false, false, kEpiY, true)
   CIDER_GEMV_CASE(false, true, kEpiY, true)
   CIDER_GEMV_CASE(true, false, kEpiY, true)
