@@ -187,14 +187,15 @@ def library_path(M: int, K: int, gs: int):
     one linear call: the same limits as gemv_fits() and launch_gemm_tc() in the
     CUDA sources (small-M GEMV up to M=16 when its activation block and a ring
     of at least four 4 KiB weight tiles fit in shared memory, preceded by the
-    per-token quantization kernel from M=4; otherwise the quantization kernel
+    per-token quantization kernel unless M == 1 or M * K <= 8192; otherwise the
+    quantization kernel
     followed by one tensor-core GEMM)."""
     if 1 <= M <= 16:
         mb = 1
         while mb < M:
             mb *= 2
         if mb * K <= 200 * 1024 and (227 * 1024 - 4096 - mb * K) // 4096 >= 4:
-            if M <= 3:   # kGemvFusedMaxM: the GEMV quantizes the rows itself
+            if M == 1 or M * K <= 8192:   # gemv_quantizes_itself()
                 return "gemv_kernel (small-M weight-streaming GEMV, fused quantization)", 1
             return "gemv_kernel (small-M weight-streaming GEMV, tensor-core form)", 2
     if gs:

@@ -110,8 +110,8 @@ cider_status_t cider_quantize_weight_int4(const float* w, int64_t N, int64_t K,
  * matmul_fused_dequant).  Quantizes x per token on the device (scratch from
  * the library's stream-ordered pool), then runs the integer GEMM with the
  * dequant fused into its store.  M <= 16 uses the weight-streaming GEMV path,
- * larger M the tensor-core GEMM (for M <= 3 the small-M kernel quantizes the
- * rows itself and needs no scratch).
+ * larger M the tensor-core GEMM (for M = 1, or M * K <= 8192, the small-M
+ * kernel quantizes the rows itself and needs no scratch).
  *   x     fp16 [M, K]
  *   qw    int8 [N, K]       (out_features x in_features, nn.Linear layout)
  *   sw    fp32 [N] (granularity CIDER_PER_CHANNEL, group_size 0)

@@ -220,13 +220,13 @@ cider_status_t run_linear(const LinearArgs& a) {
   const int gs = a.group_size;
   Scratch scratch;
   if (cider::gemv_fits(a.M, a.K)) {
-    // small M.  Up to 3 tokens the GEMV quantizes the rows itself (every CTA
-    // repeats that work, which is cheaper than a second launch for so few
-    // rows); from 4 tokens one quantization kernel writes the int8 codes first.
+    // small M: for one token or short rows the GEMV quantizes the rows itself
+    // (every CTA repeats that work, cheaper than a second launch for so few
+    // values); otherwise one quantization kernel writes the int8 codes first.
     const __half* xg = static_cast<const __half*>(a.x);
     const int8_t* qa = a.qa;
     const float* sa = a.sa;
-    if (xg && a.M >= cider::kGemvFusedMaxM + 1) {
+    if (xg && !cider::gemv_quantizes_itself(a.M, a.K)) {
       const size_t qbytes = round_up(static_cast<size_t>(a.M * a.K), 256);
       cudaError_t e = scratch_alloc(scratch, dev, qbytes + round_up(4 * a.M, 256), a.st);
       if (e != cudaSuccess) return cuda_status(e);

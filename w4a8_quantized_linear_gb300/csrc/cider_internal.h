@@ -55,9 +55,10 @@ cudaError_t launch_codes_s8_to_f16(const int8_t* qa, int64_t M, int64_t K, __hal
 // qa int8 [M, K] with scales sa [M].  group_size 0 = per channel.  Exactly
 // one of y / acc is used (by mode).
 bool gemv_fits(int64_t M, int64_t K);
-// Largest M for which the linear entry points let the GEMV quantize the
-// activation rows itself; above it a separate quantization kernel runs first.
-constexpr int64_t kGemvFusedMaxM = 3;
+// Whether the linear entry points let the GEMV quantize the activation rows
+// itself (every CTA repeats that work) rather than run a quantization kernel
+// first: for one token, or while the rows are short (measured on GB300).
+inline bool gemv_quantizes_itself(int64_t M, int64_t K) { return M == 1 || M * K <= 8192; }
 cudaError_t launch_gemv(const __half* x, const int8_t* qa, const float* sa, int64_t M, int64_t N,
                         int64_t K, const uint8_t* w, bool int4, const float* sw, int group_size,
                         int mode, __half* y, int32_t* acc, int num_sms, cudaStream_t st);
