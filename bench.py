@@ -176,7 +176,7 @@ def measured_peaks():
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "w4a8_quantized_linear_gb300", "csrc")
-    for name in ("gemm_tc.cu", "gemv.cu", "cider_device.cuh"):
+    for name in ("gemm_pair.cu", "gemm_tc.cu", "gemv.cu", "cider_device.cuh"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
