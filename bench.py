@@ -173,12 +173,18 @@ def measured_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def kernel_source_sha() -> str:
+def kernel_source_sha(names=("gemm_pair.cu", "gemm_tc.cu", "gemv.cu", "cider_device.cuh")) -> str:
+    """Hash of the kernels' CUDA sources with comments and blank lines removed,
+    so that counters taken on a kernel stay attached to it until its code
+    changes."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "w4a8_quantized_linear_gb300", "csrc")
-    for name in ("gemm_pair.cu", "gemm_tc.cu", "gemv.cu", "cider_device.cuh"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+    for name in names:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            for line in f:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 
@@ -197,7 +203,9 @@ def library_path(M: int, K: int, gs: int):
         if mb * K <= 200 * 1024 and (227 * 1024 - 4096 - mb * K) // 4096 >= 4:
             if M == 1 or M * K <= 8192:   # gemv_quantizes_itself()
                 return "gemv_kernel (small-M weight-streaming GEMV, fused quantization)", 1
-            return "gemv_kernel (small-M weight-streaming GEMV, tensor-core form)", 2
+            if M >= 4:
+                return "gemv_kernel (small-M weight-streaming GEMV, tensor-core form)", 2
+            return "gemv_kernel (small-M weight-streaming GEMV on pre-quantized rows)", 2
     if gs:
         return "gemm_tc_kernel (tcgen05 kind::f16 on exact integer codes, per-group epilogue)", 2
     return "gemm_pair_kernel (tcgen05 cta_group::2 on CTA pairs, 256x256 tiles)", 2
@@ -212,7 +220,7 @@ def ncu_traffic(workload: str):
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload)
-    if not e or e.get("kernel_source_sha") != kernel_source_sha():
+    if not e or e.get("kernel_source_sha") != kernel_source_sha(tuple(e.get("sources", ()))):
         return None
     return e.get("dram_bytes_per_launch")
 

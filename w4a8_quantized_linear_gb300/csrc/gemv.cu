@@ -4,30 +4,31 @@
 // weight bandwidth).  Unlike the page's decode kernel, the activation is
 // quantized per token here too, so results do not depend on M.
 //
-// Layout: each CTA (8 warps) keeps the quantized activation rows (MB x K int8
-// codes, rows beyond M zero) in shared memory.  In the fused form the CTA
-// quantizes the fp16 rows itself (per-token amax, IEEE scale, round-half-even
-// codes), which for decode-sized M costs far less than a separate launch.  The
-// first weight loads are issued before that staging, so HBM streaming starts
-// at once.  Weights stream with 16-byte loads: lane l of a warp takes chunks
-// l, l+32, ... of a row (16 int8 or 32 packed INT4 values per chunk), so one
-// warp load instruction covers 512 contiguous bytes; each warp keeps kRows
-// rows and D chunk loads per row in flight.  Warps may split K (KS > 1) when
-// N is too small to fill the GPU with whole rows; partial sums then meet in
-// shared memory.  Grids are sized to be resident in one wave.
+// Layout: each CTA (8 consumer warps + 1 producer warp) keeps the quantized
+// activation rows (MB x K int8 codes, rows beyond M zero) in shared memory.
+// In the fused form the CTA quantizes the fp16 rows itself (per-token amax,
+// IEEE scale, round-half-even codes), which for one token or short rows costs
+// far less than a separate launch; from 2 tokens with longer rows the codes
+// come from one quantization launch instead, so that each of the many CTAs
+// does not quantize the same rows again.  The producer warp issues the first
+// weight loads before that staging, so HBM streaming starts at once: weight
+// tiles of 16 rows x 256 bytes go by 2-D TMA into a ring of up to 8 slots.
+// Grids are sized to be resident in one wave; CTA c takes row blocks c,
+// c + grid, ...
 //
-// For 4 to 16 tokens the dot products run on the tensor
-// cores instead (mma.sync m16n8k16, fp16 operands holding the exact codes,
-// fp32 accumulation drained to int32 after every 64 codes, so every partial
-// sum stays below 2^20 and exact; INT4 codes are unpacked to int8 first):
-// each tile is split into four 64-byte quarters, one per warp, and the two
-// sets of four warps take alternate
-// tiles; the warps' partial sums meet in shared memory at the end of each
-// 16-row block.  With dp4a at these M each weight byte costs M / 4
+// For 4 to 16 tokens the dot products run on the tensor cores (mma.sync
+// m16n8k16, fp16 operands holding the exact codes, fp32 accumulation drained
+// to int32 after every 64 codes, so every partial sum stays below 2^20 and
+// exact; INT4 codes are unpacked to int8 first): each tile is split into four
+// 64-byte quarters, one per warp, and the two sets of four warps take
+// alternate tiles; the warps' partial sums meet in shared memory at the end
+// of each 16-row block.  With dp4a at these M each weight byte costs M / 4
 // instructions plus shared-memory reloads of the activations, which made the
 // kernel compute-bound well below the weight bandwidth.
 //
-// Accumulation is exact int32 (dp4a).  Per channel: the lane sums are reduced
+// For 1 or 2 tokens (dp4a form) consumer warp w owns rows 2w, 2w+1 of a
+// block; lane l works on row 2w + l/16 and its 16-byte chunk l%16 of each
+// tile.  Accumulation is exact int32 (dp4a).  Per channel: the lane sums are reduced
 // exactly and y = fp16((float(acc) * s_a) * s_w).  Per group: every chunk
 // lies inside one group; the lane's exact partial of that group is scaled by
 // s_w[n, g] and summed in fp32, y = fp16(s_a * sum) (a reassociation of the
@@ -548,8 +549,8 @@ cudaError_t dispatch_mb(const __half* x, const int8_t* qa, const float* sa, int6
                         __half* y, int32_t* acc, int num_sms, cudaStream_t st) {
   const bool pg = gs > 0;
   const bool fq = x != nullptr;
-  // tensor-core form for 4..16 tokens with int8 weights (not for the exact
-  // per-group accumulators, which keep the dp4a lanes' group reductions)
+  // tensor-core form for 4..16 tokens, int8 or int4 weights (not for the
+  // exact per-group accumulators, which keep the dp4a lanes' group reductions)
   constexpr bool kMmaMB = MB >= 4;
   if (kMmaMB && !(pg && mode == kEpiAcc) && ring_slots(MB, K, true) >= 4) {
 #define CIDER_GEMV_MMA_CASE(I4, P, E, F)                                                      \
