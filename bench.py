@@ -63,9 +63,9 @@ def parse_args():
     ap.add_argument("--bits", type=int, default=8, choices=[8, 4])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
-                    help="replay the timed steps from a CUDA graph (auto: for M <= 16, where "
-                         "one layer call is shorter than its host-side launch path)")
+    ap.add_argument("--graph", choices=["on", "off"], default="on",
+                    help="replay the timed steps from a CUDA graph (off: direct launches from "
+                         "Python, whose host-side path is longer than one call below M ~ 2048)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -344,7 +344,7 @@ def run_ours(a):
         step(i)
     torch.cuda.synchronize()
 
-    use_graph = a.graph == "on" or (a.graph == "auto" and a.M <= 16)
+    use_graph = a.graph == "on"
     graph = graph_timed = None
     per_graph = 1
     if use_graph:

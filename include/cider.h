@@ -215,6 +215,24 @@ cider_status_t cider_check_device_error(void* stream);
  * cider_check_device_error. */
 cider_status_t cider_debug_wait_timeout(int64_t max_polls, void* stream);
 
+/* Work split of the per-channel tensor-core GEMM, for inspection and tests:
+ * pure host arithmetic, no GPU needed.  For an M x N x K problem on `pairs`
+ * CTA pairs (`pairs` >= 1 stands for the device's count), the GEMM's 256 x 256
+ * output tiles are dealt whole for whole rounds, and (when that is cheaper)
+ * each remaining tile is cut along K into equal pieces on several pairs, each
+ * of which then adds up all pieces' partial sums for its own share of the
+ * tile's weight rows.  Writes info[0..5] = {pairs launched, tiles dealt whole,
+ * tiles cut, pieces per cut tile, 128-K blocks per tile, tiles} and, for every
+ * launched pair in the order it processes them, one row of seven int32 per
+ * unit: {pair, tile, first block, end block, kind (0 whole, 1 piece), first
+ * and end weight row (within the tile) that the unit dequantizes and stores}.
+ * `units` holds `capacity` rows; `count` receives the number of rows (which
+ * may exceed `capacity`: then only `capacity` are written).  Returns
+ * CIDER_ERR_INVALID_ARGUMENT for sizes < 1, pairs < 1 or NULL outputs. */
+cider_status_t cider_debug_pair_schedule(int64_t M, int64_t N, int64_t K, int pairs,
+                                         int64_t capacity, int32_t* units, int64_t* count,
+                                         int32_t* info);
+
 #ifdef __cplusplus
 }
 #endif

@@ -172,6 +172,25 @@ def test_single_layer_workload_all_rows(cider):
     assert_bits_equal(y, oracle.linear(x, qw, sw, 0, threads=8), "single layer, all rows")
 
 
+@pytest.mark.parametrize("bits", [8, 4])
+def test_whole_rounds_then_cut_tiles_all_outputs(cider, bits):
+    """A shape whose per-channel GEMM runs a whole round of 256 x 256 tiles and
+    then cuts the remaining tiles along K into pieces that add up each
+    other's partial sums: every output and every accumulator, bit for bit."""
+    M, N, K = 2560, 2048, 4096
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    info, _ = cider.cider_debug_pair_schedule(M, N, K, pairs)
+    if not (info["whole_tiles"] > 0 and info["cut_tiles"] > 0):
+        pytest.skip(f"no cut on this device: {info}")
+    x = inputs.activations(M, K, seed=123)
+    qw_dev, qw_vals, sw = make_weights(N, K, 0, bits, seed=124)
+    y = run_linear(cider, x, qw_dev, sw, 0, bits)
+    assert_bits_equal(y, oracle.linear(x, qw_vals, sw, 0, threads=8), f"cut tiles y bits={bits}")
+    qa, _ = oracle.quantize_act(x)
+    acc = run_acc(cider, qa, qw_dev, 0, bits)
+    assert_bits_equal(acc, oracle.gemm_acc(qa, qw_vals, 0), f"cut tiles acc bits={bits}")
+
+
 def test_no_device_error_left(cider):
     assert cider.cider_check_device_error() == 0
 

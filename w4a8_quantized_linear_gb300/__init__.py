@@ -58,6 +58,7 @@ def _declare(lib):
         "cider_timing_begin": ([i64], i32),
         "cider_timing_end": ([ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)], i32),
         "cider_debug_wait_timeout": ([i64, p], i32),
+        "cider_debug_pair_schedule": ([i64, i64, i64, i32, i64, p, p, p], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -249,3 +250,20 @@ def cider_timing_end():
     ms = ctypes.c_double(0.0)
     _check("cider_timing_end", _load().cider_timing_end(ctypes.byref(n), ctypes.byref(ms)))
     return int(n.value), float(ms.value)
+
+
+def cider_debug_pair_schedule(M: int, N: int, K: int, pairs: int):
+    """Work split of the per-channel tensor-core GEMM (host arithmetic only).
+    -> (info dict, list of (pair, tile, kb0, kb1, kind, row0, row1))."""
+    info = (ctypes.c_int32 * 6)()
+    count = ctypes.c_int64(0)
+    lib = _load()
+    _check("cider_debug_pair_schedule",
+           lib.cider_debug_pair_schedule(M, N, K, pairs, 0, None, ctypes.byref(count), info))
+    rows = (ctypes.c_int32 * (7 * max(count.value, 1)))()
+    _check("cider_debug_pair_schedule",
+           lib.cider_debug_pair_schedule(M, N, K, pairs, count.value, rows, ctypes.byref(count),
+                                         info))
+    keys = ("pairs", "whole_tiles", "cut_tiles", "pieces", "blocks_per_tile", "tiles")
+    units = [tuple(rows[7 * i:7 * i + 7]) for i in range(count.value)]
+    return dict(zip(keys, list(info))), units

@@ -246,21 +246,22 @@ cider_status_t run_linear(const LinearArgs& a) {
   // tensor-core path: activation codes as fp16 integers, scales, row sums of |code|
   const size_t qbytes = round_up(static_cast<size_t>(a.M * a.K) * 2, 256);
   const size_t vbytes = round_up(4 * a.M, 256);
-  const size_t wsbytes = cider::gemm_tc_workspace_bytes(a.M, a.N, a.K, gs);
-  cudaError_t e = scratch_alloc(scratch, dev, qbytes + 2 * vbytes + wsbytes, a.st);
+  const cider::GemmScratch gsc = cider::gemm_tc_scratch(a.M, a.N, a.K, gs);
+  cudaError_t e = scratch_alloc(scratch, dev, qbytes + 2 * vbytes + gsc.bytes, a.st);
   if (e != cudaSuccess) return cuda_status(e);
   uint8_t* sbase = static_cast<uint8_t*>(scratch.ptr);
   __half* q16 = reinterpret_cast<__half*>(sbase);
   int* row_l1 = reinterpret_cast<int*>(sbase + qbytes + vbytes);
-  void* ws = wsbytes ? sbase + qbytes + 2 * vbytes : nullptr;
+  uint8_t* ws = gsc.bytes ? sbase + qbytes + 2 * vbytes : nullptr;
+  int* zero = ws ? reinterpret_cast<int*>(ws + gsc.zero_offset) : nullptr;
   const float* sa = a.sa;
   if (a.x) {
     float* sscr = reinterpret_cast<float*>(sbase + qbytes);
     e = cider::launch_quant_act_f16(static_cast<const __half*>(a.x), a.M, a.K, q16, sscr, row_l1,
-                                    a.st);
+                                    zero, gsc.zero_words, a.st);
     sa = sscr;
   } else {
-    e = cider::launch_codes_s8_to_f16(a.qa, a.M, a.K, q16, row_l1, a.st);
+    e = cider::launch_codes_s8_to_f16(a.qa, a.M, a.K, q16, row_l1, zero, gsc.zero_words, a.st);
   }
   if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(timed_launch(a.st, [&] {
@@ -479,6 +480,18 @@ cider_status_t cider_debug_wait_timeout(int64_t max_polls, void* stream) {
     cider_status_t s = check_device(nullptr, nullptr);
     if (s != CIDER_OK) return s;
     return cuda_status(cider::launch_debug_wait_timeout(max_polls, static_cast<cudaStream_t>(stream)));
+  });
+}
+
+cider_status_t cider_debug_pair_schedule(int64_t M, int64_t N, int64_t K, int pairs,
+                                         int64_t capacity, int32_t* units, int64_t* count,
+                                         int32_t* info) {
+  return guarded([&] {
+    if (M < 1 || N < 1 || K < 1 || pairs < 1 || capacity < 0 || count == nullptr ||
+        info == nullptr || (capacity > 0 && units == nullptr))
+      return CIDER_ERR_INVALID_ARGUMENT;
+    cider::pair_schedule(M, N, K, pairs, capacity, units, count, info);
+    return CIDER_OK;
   });
 }
 

@@ -109,6 +109,40 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// ------------------------------------------------- flags in global memory
+// A counter that other CTAs of the same launch wait on.  Every thread that
+// wrote data the waiters will read adds 1 with release semantics (covering
+// its own earlier stores); a waiter that reads the full count with acquire
+// semantics then sees every one of those stores.
+__device__ __forceinline__ void gpu_count_release(int* counter) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(counter) : "memory");
+}
+
+__device__ __forceinline__ int gpu_load_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait until *counter >= target (same give-up rules as
+// mbar_wait_bounded).
+__device__ __forceinline__ bool gpu_count_wait_bounded(const int* counter, int target,
+                                                       volatile uint32_t* abort_flag, int* err,
+                                                       uint64_t timeout_ns) {
+  if (gpu_load_acquire(counter) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint64_t n = 1;; ++n) {
+    __nanosleep(64);
+    if (gpu_load_acquire(counter) >= target) return true;
+    if (*abort_flag) return false;
+    if ((n & 15) == 0 && global_timer_ns() - t0 > timeout_ns) {
+      *abort_flag = 1u;
+      atomicOr(err, kDevErrTimeout);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- clusters
 // Rank of this CTA in its cluster.
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -42,13 +42,14 @@ enum EpiMode : int {
 // quant.cu
 cudaError_t launch_quant_act_s8(const __half* x, int64_t M, int64_t K, int8_t* q, float* sa,
                                 cudaStream_t st);
-// fp16 codes for the tensor-core path, plus row_l1[m] = sum_k |q[m,k]|.
+// fp16 codes for the tensor-core path, plus row_l1[m] = sum_k |q[m,k]|; also
+// clears `zero_words` int32 words at `zero` (the GEMM's flags) on the way.
 cudaError_t launch_quant_act_f16(const __half* x, int64_t M, int64_t K, __half* q, float* sa,
-                                 int* row_l1, cudaStream_t st);
+                                 int* row_l1, int* zero, int zero_words, cudaStream_t st);
 cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int group_size, bool int4,
                                 uint8_t* q, float* sw, cudaStream_t st);
 cudaError_t launch_codes_s8_to_f16(const int8_t* qa, int64_t M, int64_t K, __half* out,
-                                   int* row_l1, cudaStream_t st);
+                                   int* row_l1, int* zero, int zero_words, cudaStream_t st);
 
 // gemv.cu: small-M weight-streaming path (M <= 16).  Activations either as
 // fp16 x [M, K] (quantized inside the kernel; x != nullptr) or as codes
@@ -67,18 +68,27 @@ cudaError_t launch_gemv(const __half* x, const int8_t* qa, const float* sa, int6
 // integers [M, K]; row_l1[m] = sum_k |code| (used by the per-channel kernel
 // to decide per tile whether one fp32 accumulation over all of K is exact).
 // Per channel (group_size 0) it runs the CTA-pair kernel of gemm_pair.cu,
-// split over K when the output tiles cannot occupy the GPU and `workspace`
-// (gemm_tc_workspace_bytes(...) bytes, or null to never split) allows it.
-size_t gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size);
+// which shares the blocks of the last partial round of tiles among all CTA
+// pairs when `workspace` (gemm_tc_scratch(...).bytes, or null to deal every
+// tile whole) allows it.
+struct GemmScratch {
+  size_t bytes = 0;        // workspace size (0: none wanted)
+  size_t zero_offset = 0;  // byte offset of int32 words that must be zero at launch
+  int zero_words = 0;
+};
+GemmScratch gemm_tc_scratch(int64_t M, int64_t N, int64_t K, int group_size);
 cudaError_t launch_gemm_tc(const __half* qa16, const float* sa, const int* row_l1, int64_t M,
                            int64_t N, int64_t K, const uint8_t* w, bool int4, const float* sw,
                            int group_size, int mode, __half* y, int32_t* acc, void* workspace,
                            int num_sms, cudaStream_t st);
 // gemm_pair.cu: per-channel tensor-core path on CTA pairs (see launch_gemm_tc).
-size_t gemm_pair_workspace_bytes(int64_t M, int64_t N, int64_t K);
+GemmScratch gemm_pair_scratch(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_pair(const __half* qa16, const float* sa, const int* row_l1, int64_t M,
                              int64_t N, int64_t K, const uint8_t* w, bool int4, const float* sw,
                              int mode, __half* y, int32_t* acc, void* workspace, cudaStream_t st);
+// Host copy of the pair GEMM's work split (see cider_debug_pair_schedule).
+void pair_schedule(int64_t M, int64_t N, int64_t K, int pairs, int64_t capacity, int32_t* units,
+                   int64_t* count, int32_t* info);
 cudaError_t read_and_clear_device_error(int* value);
 // Device address of the library's error word on the current device.
 cudaError_t device_error_word(int** ptr);

@@ -47,12 +47,21 @@
 //               packed [128 n][32 B]) into a separate 4-slot ring, one
 //               sub-tile per slot, running ahead of the conversion.
 //
-// Split-K: when the output tiles alone cannot occupy the GPU's CTA pairs (M
-// up to ~1000 tokens), each tile's K range is cut into ks slices processed by
-// different pairs.  A slice's accumulator is an exact integer (the per-tile
-// bound below holds for any part of K); it is stored as int32 into a
-// workspace [ks][M][N], and split_combine_kernel adds the ks partials in
-// int32 (exact) and applies the dequant.
+// Work split: with P pairs, whole tiles are dealt round-robin for
+// floor(tiles / P) rounds.  When the remaining r tiles would leave most pairs
+// idle in a last round, each of them is cut along K into s = floor(P / r)
+// equal pieces (at least four 128-K blocks each) on s pairs: 640 tiles on 76
+// pairs run as 8 whole rounds plus 32 tiles in 2 halves on 64 pairs, instead
+// of 9 rounds.  A piece's accumulator is an exact integer (the per-tile bound
+// below holds for any part of K).  Each pair stores it as int32 into its own
+// workspace slot, in a layout where the 32 lanes of a warp touch 512
+// consecutive bytes, and raises its slot's flag; it then waits for the flags
+// of the tile's other pieces, adds up all s partials for its own 1/s of the
+// tile's weight rows (exact int32) and dequantizes and stores that part of
+// y.  Every pair writes before it waits, so the waits cannot cycle; the
+// pieces of a tile run at the same time on co-resident pairs (the grid never
+// exceeds the pairs the GPU holds at once).  The flags are zeroed by the
+// activation-quantization kernel that precedes every launch.
 //
 // Exactness per tile: every partial sum of token m is bounded by
 // qmax_w * sum_k |q_a[m,k]| (qmax_w = 127 INT8, 8 INT4).  When that bound is
@@ -117,9 +126,12 @@ static_assert(kPSubBytes % 1024 == 0, "sub-tiles must keep 1024-byte alignment f
 struct PairArgs {
   int M, N, K;
   int num_m_tiles, num_tiles;
-  int ks;          // K slices per tile (split-K when the tiles alone cannot fill the GPU)
-  int num_units;   // num_tiles * ks
-  int32_t* ws;     // ks > 1: partial accumulators [ks][M][N]
+  int nkb;          // 128-K blocks per tile
+  int full_tiles;   // tiles [0, full_tiles) are dealt whole, round-robin over the pairs
+  int sk_tiles;     // tiles [full_tiles, full_tiles + sk_tiles) are cut into pieces
+  int sk_split;     // s: pieces per cut tile; pair c < sk_tiles * s takes piece c % s of tile c / s
+  int4* part;       // partials [pair][2 CTAs][64 x 16-byte column groups][128 tokens]
+  int* flags;       // [pair][2 CTAs][4 lane quarters], zero at launch
   const float* sa;
   const float* sw;
   __half* y;
@@ -128,6 +140,39 @@ struct PairArgs {
   int l1_limit;
   int* err;
 };
+
+// One unit of a pair's work: blocks [kb0, kb1) of a tile.
+enum : int {
+  kUnitWhole = 0,   // the whole tile: dequantize and store
+  kUnitPiece = 1,   // piece kb0..kb1 of a cut tile: store the partial, then reduce a 1/s slice
+};
+struct PUnit {
+  int tile, kb0, kb1, kind;
+};
+
+__host__ __device__ __forceinline__ int pair_whole_units(const PairArgs& p, int c, int P) {
+  return c < p.full_tiles ? (p.full_tiles - 1 - c) / P + 1 : 0;
+}
+
+// Number of units of pair c (of P), and the i-th of them.  Every role of
+// both CTAs walks the same sequence.
+__host__ __device__ __forceinline__ int pair_num_units(const PairArgs& p, int c, int P) {
+  return pair_whole_units(p, c, P) + (c < p.sk_tiles * p.sk_split ? 1 : 0);
+}
+
+__host__ __device__ __forceinline__ PUnit pair_unit(const PairArgs& p, int c, int P, int i) {
+  if (i < pair_whole_units(p, c, P)) return PUnit{c + i * P, 0, p.nkb, kUnitWhole};
+  const int k = c % p.sk_split;
+  return PUnit{p.full_tiles + c / p.sk_split, k * p.nkb / p.sk_split, (k + 1) * p.nkb / p.sk_split,
+               kUnitPiece};
+}
+
+// 16-byte column groups [j0, j1) of the tile (4 weight rows each, in pairs so
+// that groups of 8 outputs stay whole) that piece k of s reduces and stores.
+__host__ __device__ __forceinline__ void piece_slice(int k, int s, int* j0, int* j1) {
+  *j0 = 2 * ((32 * k) / s);
+  *j1 = 2 * ((32 * (k + 1)) / s);
+}
 
 // Whole warp: is every token of token tile mt within the exactness bound?
 __device__ __forceinline__ bool pair_tile_fast(const PairArgs& a, int mt, int lane) {
@@ -142,14 +187,14 @@ __device__ __forceinline__ bool pair_tile_fast(const PairArgs& a, int mt, int la
 }
 
 // y[m, n0 .. n0 + 7] = fp16((acc * s_a[m]) * s_w[n]) from eight exact
-// accumulator values, one 16-byte store.
-__device__ __forceinline__ void store8_y(const PairArgs& p, int m, float sam, int n0, const float* f) {
+// accumulator values and the eight weight scales, one 16-byte store.
+__device__ __forceinline__ void store8_y(const PairArgs& p, int m, float sam, int n0, const float* f,
+                                         const float (&w)[8]) {
   uint32_t h[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const __half lo = __float2half_rn(__fmul_rn(__fmul_rn(f[2 * i], sam), __ldg(p.sw + n0 + 2 * i)));
-    const __half hi =
-        __float2half_rn(__fmul_rn(__fmul_rn(f[2 * i + 1], sam), __ldg(p.sw + n0 + 2 * i + 1)));
+    const __half lo = __float2half_rn(__fmul_rn(__fmul_rn(f[2 * i], sam), w[2 * i]));
+    const __half hi = __float2half_rn(__fmul_rn(__fmul_rn(f[2 * i + 1], sam), w[2 * i + 1]));
     h[i] = static_cast<uint32_t>(__half_as_ushort(lo)) |
            (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
   }
@@ -219,15 +264,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   cluster_sync_all();   // barriers of both CTAs initialised, tensor memory held
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + C::kBarOffset + 8 * C::kNumBars);
-  const int nkb = (p.K + kPBK - 1) / kPBK;
+  const int nu = pair_num_units(p, cid, nclusters);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint32_t ready_leader0 = mapa_shared(ready_bar(0), 0);
     int it = 0;
-    for (int unit = cid; unit < p.num_units; unit += nclusters) {
-      const int tile = unit / p.ks, slice = unit % p.ks;
-      const int kb0 = slice * nkb / p.ks, kb1 = (slice + 1) * nkb / p.ks;
+    for (int ui = 0; ui < nu; ++ui) {
+      const PUnit u = pair_unit(p, cid, nclusters, ui);
+      const int tile = u.tile, kb0 = u.kb0, kb1 = u.kb1;
       const int mt = tile % p.num_m_tiles;
       const int passes = pair_tile_fast(p, mt, lane) ? 1 : kPSlowPasses;
       if (lane == 0) {
@@ -253,9 +298,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       constexpr uint32_t idesc_fast = idesc_f16_f32(kPTileM, kPTileN);
       constexpr uint32_t idesc_slow = idesc_f16_f32(kPTileM, kPTileN / kPSlowPasses);
       int it = 0, ch = 0;
-      for (int unit = cid; unit < p.num_units; unit += nclusters) {
-        const int tile = unit / p.ks, slice = unit % p.ks;
-        const int kb0 = slice * nkb / p.ks, kb1 = (slice + 1) * nkb / p.ks;
+      for (int ui = 0; ui < nu; ++ui) {
+        const PUnit u = pair_unit(p, cid, nclusters, ui);
+        const int tile = u.tile, kb0 = u.kb0, kb1 = u.kb1;
         const int mt = tile % p.num_m_tiles;
         const bool fast = pair_tile_fast(p, mt, lane);
         if (lane == 0) {
@@ -313,9 +358,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const int row = (warp & 3) * 32 + lane;
     const uint32_t ready_leader0 = mapa_shared(ready_bar(0), 0);
     int it = 0;
-    for (int unit = cid; unit < p.num_units; unit += nclusters) {
-      const int tile = unit / p.ks, slice = unit % p.ks;
-      const int kb0 = slice * nkb / p.ks, kb1 = (slice + 1) * nkb / p.ks;
+    for (int ui = 0; ui < nu; ++ui) {
+      const PUnit u = pair_unit(p, cid, nclusters, ui);
+      const int tile = u.tile, kb0 = u.kb0, kb1 = u.kb1;
       const int mt = tile % p.num_m_tiles;
       const int passes = pair_tile_fast(p, mt, lane) ? 1 : kPSlowPasses;
       for (int pass = 0; pass < passes; ++pass) {
@@ -381,9 +426,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   } else if (warp == kPW8Warp) {
     // ------------------------------------------------------------ weight-code producer
     int it = 0;
-    for (int unit = cid; unit < p.num_units; unit += nclusters) {
-      const int tile = unit / p.ks, slice = unit % p.ks;
-      const int kb0 = slice * nkb / p.ks, kb1 = (slice + 1) * nkb / p.ks;
+    for (int ui = 0; ui < nu; ++ui) {
+      const PUnit u = pair_unit(p, cid, nclusters, ui);
+      const int tile = u.tile, kb0 = u.kb0, kb1 = u.kb1;
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
       const int passes = pair_tile_fast(p, mt, lane) ? 1 : kPSlowPasses;
       if (lane == 0) {
@@ -411,27 +456,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const int q = warp & 3;            // tensor-memory lane quarter of this warp
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
-    const bool split = p.ks > 1;
     int ch = 0;
-    for (int unit = cid; unit < p.num_units; unit += nclusters) {
-      const int tile = unit / p.ks, slice = unit % p.ks;
-      const int kb0 = slice * nkb / p.ks, kb1 = (slice + 1) * nkb / p.ks;
+    for (int ui = 0; ui < nu; ++ui) {
+      const PUnit u = pair_unit(p, cid, nclusters, ui);
+      const int tile = u.tile, kb0 = u.kb0, kb1 = u.kb1;
       const int nch = (kb1 - kb0 + kPChunkKB - 1) / kPChunkKB;
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
       const bool fast = pair_tile_fast(p, mt, lane);
-      const int m = mt * kPTileM + static_cast<int>(rank) * kPHalf + q * 32 + lane;
+      const int row = q * 32 + lane;   // token of this thread within the CTA's 128
+      const int m = mt * kPTileM + static_cast<int>(rank) * kPHalf + row;
       const bool mvalid = m < p.M;
       const float sam = (EPI == kEpiY && mvalid) ? __ldg(p.sa + m) : 0.0f;
       const int n_tile = nt * kPTileN;
-      int32_t* wrow = split ? p.ws + (static_cast<int64_t>(slice) * p.M + m) * p.N : nullptr;
-      // eight exact accumulator values of weight rows n0 .. n0 + 7: the
-      // result, or this slice's partial sums
-      auto emit8 = [&](int n0, const int (&iv)[8]) {
-        if (split) {
-          int4* d = reinterpret_cast<int4*>(wrow + n0);
-          d[0] = make_int4(iv[0], iv[1], iv[2], iv[3]);
-          d[1] = make_int4(iv[4], iv[5], iv[6], iv[7]);
-        } else if (EPI == kEpiAcc) {
+      const bool piece = u.kind == kUnitPiece;
+      // partial slot of a pair: 16-byte column group j of this thread's token
+      // row at [j][row], so that a warp's lanes touch consecutive 16 bytes
+      auto slot = [&](int pair) {
+        return p.part + (static_cast<int64_t>(pair) * 2 + rank) * (kPTileN / 4) * kPHalf + row;
+      };
+      // The tile's 256 weight scales, 8 per lane (lane l: weight rows 8 l ..
+      // 8 l + 7), handed to the lanes that need them by shuffles: every lane
+      // uses all 256 scales, and loading each one per lane from the cache
+      // made the epilogue the slower half of the pipeline.
+      float swr[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int n = n_tile + lane * 8 + i;
+        swr[i] = (EPI == kEpiY && n < p.N) ? __ldg(p.sw + n) : 0.0f;
+      }
+      // scales of tile columns col .. col + 7 (col % 8 == 0); the whole warp calls this
+      auto scales8 = [&](int col, float (&w)[8]) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = __shfl_sync(0xffffffffu, swr[i], col >> 3);
+      };
+      // dequantize and store eight exact accumulator values of weight rows n0 .. n0 + 7
+      auto store8 = [&](int n0, const int (&iv)[8], const float (&w)[8]) {
+        if (EPI == kEpiAcc) {
           const int64_t off = static_cast<int64_t>(m) * p.N + n0;
 #pragma unroll
           for (int i = 0; i < 8; ++i) p.acc[off + i] = iv[i];
@@ -439,7 +499,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           float f[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) f[i] = __int2float_rn(iv[i]);
-          store8_y(p, m, sam, n0, f);
+          store8_y(p, m, sam, n0, f, w);
+        }
+      };
+      // eight exact accumulator values of tile columns col .. col + 7: the
+      // result, or this piece's partial sums.  The whole warp calls this.
+      auto emit8 = [&](int col, const int (&iv)[8]) {
+        const int n0 = n_tile + col;
+        if (piece) {
+          if (mvalid && n0 < p.N) {   // N % 8 == 0: a group of 8 is all in or all out
+            int4* d = slot(cid) + (col >> 2) * kPHalf;
+            d[0] = make_int4(iv[0], iv[1], iv[2], iv[3]);
+            d[kPHalf] = make_int4(iv[4], iv[5], iv[6], iv[7]);
+          }
+        } else {
+          float w[8];
+          if (EPI == kEpiY) scales8(col, w);
+          if (mvalid && n0 < p.N) store8(n0, iv, w);
         }
       };
       if (fast) {
@@ -454,17 +530,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + b * kPAccCols + c8 * 32, v);
           tmem_wait_ld();
-          if (mvalid) {
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              const int n0 = n_tile + c8 * 32 + g * 8;
-              if (n0 < p.N) {   // N % 8 == 0: a group of 8 is all in or all out
-                int iv[8];
+          for (int g = 0; g < 4; ++g) {
+            int iv[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) iv[i] = __float2int_rn(__uint_as_float(v[g * 8 + i]));
-                emit8(n0, iv);
-              }
-            }
+            for (int i = 0; i < 8; ++i) iv[i] = __float2int_rn(__uint_as_float(v[g * 8 + i]));
+            emit8(c8 * 32 + g * 8, iv);
           }
         }
         tc_fence_before();
@@ -494,16 +565,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(acce_leader0 + 8u * b);
           }
-          if (!mvalid) continue;
           // N = 64 pass: column j is weight row 32 pass + (j % 32) of CTA j / 32's 128
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
-            const int n0 = n_tile + (g >> 2) * kPHalf + pass * 32 + (g & 3) * 8;
-            if (n0 < p.N) {
+            int iv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) iv[i] = isum[g * 8 + i];
+            emit8((g >> 2) * kPHalf + pass * 32 + (g & 3) * 8, iv);
+          }
+        }
+      }
+      if (piece) {
+        // every lane counts its own stores of the partial; the other pieces'
+        // warps of the same CTA rank and lane quarter wait for all 32
+        gpu_count_release(p.flags + (cid * 2 + rank) * 4 + q);
+        const int s = p.sk_split, k = cid % s, c0 = cid - k;
+        for (int kk = 0; kk < s; ++kk)
+          if (kk != k && !__all_sync(0xffffffffu, gpu_count_wait_bounded(
+                                                      p.flags + ((c0 + kk) * 2 + rank) * 4 + q, 32,
+                                                      abort_flag, err, kPWaitNs)))
+            goto done;
+        int j0, j1;
+        piece_slice(k, s, &j0, &j1);
+        // up to 8 column groups (32 weight rows) at a time, two pieces' loads
+        // in flight; the slots have room for every token row of the tile, so
+        // all lanes load (rows past M are summed but not stored)
+#pragma unroll 1
+        for (int jb = j0; jb < j1; jb += 8) {
+          const int nj = j1 - jb;
+          int sum[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sum[i] = 0;
+#pragma unroll 1
+          for (int kk = 0; kk < s; kk += 2) {
+            const int4* src0 = slot(c0 + kk) + jb * kPHalf;
+            const int4* src1 = slot(c0 + (kk + 1 < s ? kk + 1 : kk)) + jb * kPHalf;
+            const bool two = kk + 1 < s;
+            int4 t0[8], t1[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int ii = i < nj ? i : 0;   // past the slice: reload group 0, unused
+              t0[i] = __ldcg(src0 + ii * kPHalf);
+              t1[i] = __ldcg(src1 + ii * kPHalf);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              if (!two) t1[i] = make_int4(0, 0, 0, 0);
+              sum[4 * i + 0] += t0[i].x + t1[i].x;
+              sum[4 * i + 1] += t0[i].y + t1[i].y;
+              sum[4 * i + 2] += t0[i].z + t1[i].z;
+              sum[4 * i + 3] += t0[i].w + t1[i].w;
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (2 * g < nj) {   // warp-uniform
+              const int col = (jb + 2 * g) * 4;
+              float w[8];
+              if (EPI == kEpiY) scales8(col, w);
               int iv[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) iv[i] = isum[g * 8 + i];
-              emit8(n0, iv);
+              for (int i = 0; i < 8; ++i) iv[i] = sum[8 * g + i];
+              if (mvalid && n_tile + col < p.N) store8(n_tile + col, iv, w);
             }
           }
         }
@@ -528,49 +651,6 @@ done:
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem, kPTmemCols);
-  }
-}
-
-// Split-K epilogue: y[m, n] (or acc) from the ks exact int32 partials of
-// ws [ks][M][N]; one thread per 8 consecutive outputs of a row.
-template <int EPI>
-__global__ void __launch_bounds__(256) split_combine_kernel(const int32_t* __restrict__ ws, int ks,
-                                                            int M, int N, const float* __restrict__ sa,
-                                                            const float* __restrict__ sw,
-                                                            __half* __restrict__ y,
-                                                            int32_t* __restrict__ acc) {
-  const int64_t groups = static_cast<int64_t>(M) * (N / 8);
-  const int64_t plane = static_cast<int64_t>(M) * N;
-  for (int64_t gi = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; gi < groups;
-       gi += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t off = gi * 8;
-    const int m = static_cast<int>(off / N);
-    const int n0 = static_cast<int>(off % N);
-    int iv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-#pragma unroll 4
-    for (int sl = 0; sl < ks; ++sl) {
-      const int4* src = reinterpret_cast<const int4*>(ws + sl * plane + off);
-      const int4 a0 = __ldcs(src), a1 = __ldcs(src + 1);
-      iv[0] += a0.x; iv[1] += a0.y; iv[2] += a0.z; iv[3] += a0.w;
-      iv[4] += a1.x; iv[5] += a1.y; iv[6] += a1.z; iv[7] += a1.w;
-    }
-    if (EPI == kEpiAcc) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[off + i] = iv[i];
-    } else {
-      const float sam = __ldg(sa + m);
-      uint32_t h[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __half lo = __float2half_rn(
-            __fmul_rn(__fmul_rn(__int2float_rn(iv[2 * i]), sam), __ldg(sw + n0 + 2 * i)));
-        const __half hi = __float2half_rn(
-            __fmul_rn(__fmul_rn(__int2float_rn(iv[2 * i + 1]), sam), __ldg(sw + n0 + 2 * i + 1)));
-        h[i] = static_cast<uint32_t>(__half_as_ushort(lo)) |
-               (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
-      }
-      *reinterpret_cast<uint4*>(y + off) = make_uint4(h[0], h[1], h[2], h[3]);
-    }
   }
 }
 
@@ -609,54 +689,118 @@ cudaError_t pair_max_clusters(int* out) {
   return cudaSuccess;
 }
 
-// K slices per tile: 1 when the tiles fill the pairs; otherwise the split
-// that minimises (rounds of units over the pairs) x (stages per slice) plus
-// the cost of the partial sums (written, read back and combined), keeping at
-// least two 128-K stages per slice and at most 8 slices.
-int pair_split(int64_t M, int64_t N, int64_t K, int nc) {
-  const int64_t tiles = ((M + kPTileM - 1) / kPTileM) * ((N + kPTileN - 1) / kPTileN);
-  const int64_t nkb = (K + kPBK - 1) / kPBK;
-  if (tiles >= nc || nkb < 4) return 1;
-  // in units of one pipeline stage of one pair (~0.5 us): a combine launch
-  // costs ~6 stages, each tile-slice of partials ~0.25 stage of traffic
-  int best = 1;
-  double best_cost = static_cast<double>(nkb);
-  for (int ks = 2; ks <= 8 && ks <= nkb / 2; ++ks) {
-    const int64_t rounds = (tiles * ks + nc - 1) / nc;
-    const double cost = static_cast<double>(rounds * ((nkb + ks - 1) / ks)) + 6.0 +
-                        0.25 * static_cast<double>(tiles * ks) * static_cast<double>(M < kPTileM ? M : kPTileM) / kPTileM;
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = ks;
-    }
-  }
-  return best;
+// Host side of the work split described at the top of this file.  Measured
+// on GB300: after whole rounds, a last partial round of whole tiles runs
+// faster than a full one (fewer pairs share the caches and HBM), so cutting
+// it pays only when it saves many blocks (long K: 4096 x 2560 x 10240 went
+// from 160 to 128 us; 4096 x 10240 x 2560, halves of 10 blocks, lost 2 %).
+constexpr int kSkMinBlocks = 4;        // shortest piece worth giving a pair, in 128-K blocks
+constexpr int kSkFixupBlocks = 2;      // storing, waiting for and adding partials, in blocks
+constexpr int kSkAfterRoundsBlocks = 24;   // extra cost of cutting after whole rounds
+
+struct PairPlan {
+  int num_m_tiles, num_tiles, nkb;
+  int clusters;     // pairs launched (P)
+  int full_tiles;   // tiles dealt whole
+  int sk_tiles;     // tiles cut into pieces (0: none)
+  int sk_split;     // pieces per cut tile
+};
+
+// Whole rounds of tiles; then, when it is cheaper by the cost below (in units
+// of one 128-K block of one pair), the r remaining tiles in s = P / r pieces
+// each.  `allow_sk` false (no workspace) deals every tile whole.
+PairPlan pair_plan(int64_t M, int64_t N, int64_t K, int nc, bool allow_sk) {
+  PairPlan pl;
+  pl.num_m_tiles = static_cast<int>((M + kPTileM - 1) / kPTileM);
+  pl.num_tiles = pl.num_m_tiles * static_cast<int>((N + kPTileN - 1) / kPTileN);
+  pl.nkb = static_cast<int>((K + kPBK - 1) / kPBK);
+  pl.clusters = pl.num_tiles < nc ? pl.num_tiles : nc;
+  pl.full_tiles = pl.num_tiles;
+  pl.sk_tiles = 0;
+  pl.sk_split = 1;
+  if (!allow_sk || nc < 2) return pl;
+  const int rounds = pl.num_tiles / nc, rem = pl.num_tiles % nc;
+  if (rem == 0) return pl;
+  int split = nc / rem;
+  if (split > pl.nkb / kSkMinBlocks) split = pl.nkb / kSkMinBlocks;
+  if (split < 2) return pl;
+  const int64_t cost_whole = static_cast<int64_t>(rounds + 1) * pl.nkb;
+  const int64_t cost_sk = static_cast<int64_t>(rounds) * pl.nkb + (pl.nkb + split - 1) / split +
+                          kSkFixupBlocks + (rounds > 0 ? kSkAfterRoundsBlocks : 0);
+  if (cost_sk >= cost_whole) return pl;
+  pl.full_tiles = rounds * nc;
+  pl.sk_tiles = rem;
+  pl.sk_split = split;
+  pl.clusters = rounds > 0 ? nc : rem * split;
+  return pl;
 }
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
 template <bool INT4, int EPI>
 cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmW, const PairArgs& a,
-                        int nc, cudaStream_t st) {
+                        int clusters, cudaStream_t st) {
   using C = PCfg<INT4>;
   auto kern = gemm_pair_kernel<INT4, EPI>;
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::kSmemBytes,
                                           attr_done);
   if (e != cudaSuccess) return e;
-  const int clusters = a.num_units < nc ? a.num_units : nc;
   kern<<<2 * clusters, kPThreads, C::kSmemBytes, st>>>(tmX, tmW, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t gemm_pair_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+void pair_schedule(int64_t M, int64_t N, int64_t K, int pairs, int64_t capacity, int32_t* units,
+                   int64_t* count, int32_t* info) {
+  const PairPlan pl = pair_plan(M, N, K, pairs, true);
+  PairArgs a{};
+  a.num_m_tiles = pl.num_m_tiles;
+  a.num_tiles = pl.num_tiles;
+  a.nkb = pl.nkb;
+  a.full_tiles = pl.full_tiles;
+  a.sk_tiles = pl.sk_tiles;
+  a.sk_split = pl.sk_split;
+  info[0] = pl.clusters;
+  info[1] = pl.full_tiles;
+  info[2] = pl.sk_tiles;
+  info[3] = pl.sk_split;
+  info[4] = pl.nkb;
+  info[5] = pl.num_tiles;
+  int64_t n = 0;
+  for (int c = 0; c < pl.clusters; ++c) {
+    const int nu = pair_num_units(a, c, pl.clusters);
+    for (int i = 0; i < nu; ++i, ++n) {
+      if (n >= capacity) continue;
+      const PUnit u = pair_unit(a, c, pl.clusters, i);
+      int j0 = 0, j1 = kPTileN / 4;
+      if (u.kind == kUnitPiece) piece_slice(c % pl.sk_split, pl.sk_split, &j0, &j1);
+      int32_t* r = units + 7 * n;
+      r[0] = c;
+      r[1] = u.tile;
+      r[2] = u.kb0;
+      r[3] = u.kb1;
+      r[4] = u.kind;
+      r[5] = j0 * 4;   // weight rows of the tile this unit dequantizes and stores
+      r[6] = j1 * 4;
+    }
+  }
+  *count = n;
+}
+
+GemmScratch gemm_pair_scratch(int64_t M, int64_t N, int64_t K) {
+  GemmScratch sc;
   int nc = 0;
-  if (pair_max_clusters(&nc) != cudaSuccess) return 0;
-  const int ks = pair_split(M, N, K, nc);
-  if (ks <= 1) return 0;
-  return round256(static_cast<size_t>(ks) * M * N * 4);
+  if (pair_max_clusters(&nc) != cudaSuccess) return sc;
+  const PairPlan pl = pair_plan(M, N, K, nc, true);
+  if (pl.sk_tiles == 0) return sc;
+  const int pieces = pl.sk_tiles * pl.sk_split;
+  const size_t part_bytes = static_cast<size_t>(pieces) * 2 * kPHalf * kPTileN * 4;
+  sc.zero_offset = round256(part_bytes);
+  sc.zero_words = pieces * 2 * 4;
+  sc.bytes = sc.zero_offset + round256(static_cast<size_t>(sc.zero_words) * 4);
+  return sc;
 }
 
 cudaError_t launch_gemm_pair(const __half* qa16, const float* sa, const int* row_l1, int64_t M,
@@ -671,18 +815,24 @@ cudaError_t launch_gemm_pair(const __half* qa16, const float* sa, const int* row
                           int4 ? kPSubK / 2 : kPSubK, kPHalf,
                           int4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
+  int nc = 0;
+  cudaError_t e = pair_max_clusters(&nc);
+  if (e != cudaSuccess) return e;
+  const PairPlan pl = pair_plan(M, N, K, nc, workspace != nullptr);
   PairArgs a;
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
-  a.num_m_tiles = static_cast<int>((M + kPTileM - 1) / kPTileM);
-  a.num_tiles = a.num_m_tiles * static_cast<int>((N + kPTileN - 1) / kPTileN);
-  int nc = 0;
-  cudaError_t e = pair_max_clusters(&nc);
-  if (e != cudaSuccess) return e;
-  a.ks = workspace ? pair_split(M, N, K, nc) : 1;
-  a.num_units = a.num_tiles * a.ks;
-  a.ws = a.ks > 1 ? static_cast<int32_t*>(workspace) : nullptr;
+  a.num_m_tiles = pl.num_m_tiles;
+  a.num_tiles = pl.num_tiles;
+  a.nkb = pl.nkb;
+  a.full_tiles = pl.full_tiles;
+  a.sk_tiles = pl.sk_tiles;
+  a.sk_split = pl.sk_split;
+  a.part = pl.sk_tiles ? static_cast<::int4*>(workspace) : nullptr;
+  a.flags = pl.sk_tiles ? reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) +
+                                                 gemm_pair_scratch(M, N, K).zero_offset)
+                        : nullptr;
   a.sa = sa;
   a.sw = sw;
   a.y = y;
@@ -692,19 +842,10 @@ cudaError_t launch_gemm_pair(const __half* qa16, const float* sa, const int* row
   e = device_error_word(&a.err);
   if (e != cudaSuccess) return e;
   if (int4)
-    e = mode == kEpiY ? launch_pair<true, kEpiY>(tmX, tmW, a, nc, st)
-                      : launch_pair<true, kEpiAcc>(tmX, tmW, a, nc, st);
-  else
-    e = mode == kEpiY ? launch_pair<false, kEpiY>(tmX, tmW, a, nc, st)
-                      : launch_pair<false, kEpiAcc>(tmX, tmW, a, nc, st);
-  if (e != cudaSuccess || a.ks == 1) return e;
-  const int64_t groups = M * (N / 8);
-  const int blocks = static_cast<int>((groups + 255) / 256 < 4096 ? (groups + 255) / 256 : 4096);
-  if (mode == kEpiY)
-    split_combine_kernel<kEpiY><<<blocks, 256, 0, st>>>(a.ws, a.ks, a.M, a.N, sa, sw, y, acc);
-  else
-    split_combine_kernel<kEpiAcc><<<blocks, 256, 0, st>>>(a.ws, a.ks, a.M, a.N, sa, sw, y, acc);
-  return cudaGetLastError();
+    return mode == kEpiY ? launch_pair<true, kEpiY>(tmX, tmW, a, pl.clusters, st)
+                         : launch_pair<true, kEpiAcc>(tmX, tmW, a, pl.clusters, st);
+  return mode == kEpiY ? launch_pair<false, kEpiY>(tmX, tmW, a, pl.clusters, st)
+                       : launch_pair<false, kEpiAcc>(tmX, tmW, a, pl.clusters, st);
 }
 
 }  // namespace cider

@@ -425,8 +425,8 @@ cudaError_t launch_gemm_tc(const __half* qa16, const float* sa, const int* row_l
                        : launch_tc<false, true, kEpiAcc>(tmA, tmB, a, num_sms, st);
 }
 
-size_t gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size) {
-  return group_size == 0 ? gemm_pair_workspace_bytes(M, N, K) : 0;
+GemmScratch gemm_tc_scratch(int64_t M, int64_t N, int64_t K, int group_size) {
+  return group_size == 0 ? gemm_pair_scratch(M, N, K) : GemmScratch{};
 }
 
 cudaError_t device_error_word(int** ptr) {

@@ -125,10 +125,11 @@ extern "C" cider_status_t cider_w8a8_linear_noalloc(const void* x, int64_t M, in
       __half* q16 = reinterpret_cast<__half*>(base);
       float* sa = reinterpret_cast<float*>(base + qbytes);
       int* row_l1 = reinterpret_cast<int*>(base + qbytes + vbytes);
-      e = cider::launch_quant_act_f16(static_cast<const __half*>(x), M, K, q16, sa, row_l1, st);
-      if (e == cudaSuccess)
+      e = cider::launch_quant_act_f16(static_cast<const __half*>(x), M, K, q16, sa, row_l1,
+                                      nullptr, 0, st);
+      if (e == cudaSuccess)   // no workspace: every output tile is computed whole by one CTA pair
         e = cider::launch_gemm_tc(q16, sa, row_l1, M, N, K, w, false, sw, group_size, cider::kEpiY,
-                                  yh, nullptr, /*workspace: never split*/ nullptr, sms, st);
+                                  yh, nullptr, nullptr, sms, st);
     }
     if (e != cudaSuccess) {
       cudaGetLastError();

@@ -87,16 +87,26 @@ __device__ __forceinline__ int block_sum_128(int v, int* red) {
   return red[0] + red[1] + red[2] + red[3];
 }
 
+// The first CTA clears a small array for the kernel that follows on the
+// stream (the GEMM's flags), which saves a separate launch.
+__device__ __forceinline__ void clear_words(int* zero, int n) {
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n; i += blockDim.x) zero[i] = 0;
+}
+
 // One CTA of 128 threads per row; the row stays in registers between the
 // amax pass and the quantization pass (VPT 16-byte vectors per thread).
 template <typename OutT, int VPT>
 __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const __half* __restrict__ x,
                                                                   int64_t K, OutT* __restrict__ q,
                                                                   float* __restrict__ sa,
-                                                                  int* __restrict__ row_l1) {
+                                                                  int* __restrict__ row_l1,
+                                                                  int* __restrict__ zero,
+                                                                  int zero_words) {
   __shared__ float red[4];
   __shared__ int ired[4];
   const int64_t m = blockIdx.x;
+  clear_words(zero, zero_words);
   const uint4* row = reinterpret_cast<const uint4*>(x + m * K);
   const int nvec = static_cast<int>(K >> 3);
   uint4 v[VPT];
@@ -135,10 +145,13 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_long_kernel(const __h
                                                                        int64_t K,
                                                                        OutT* __restrict__ q,
                                                                        float* __restrict__ sa,
-                                                                       int* __restrict__ row_l1) {
+                                                                       int* __restrict__ row_l1,
+                                                                       int* __restrict__ zero,
+                                                                       int zero_words) {
   __shared__ float red[4];
   __shared__ int ired[4];
   const int64_t m = blockIdx.x;
+  clear_words(zero, zero_words);
   const uint4* row = reinterpret_cast<const uint4*>(x + m * K);
   const int64_t nvec = K >> 3;
   __half2 amax2 = __float2half2_rn(0.0f);
@@ -164,28 +177,28 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_long_kernel(const __h
 
 template <typename OutT>
 cudaError_t launch_quant_act(const __half* x, int64_t M, int64_t K, OutT* q, float* sa,
-                             int* row_l1, cudaStream_t st) {
+                             int* row_l1, int* zero, int zero_words, cudaStream_t st) {
   const int64_t nvec = K / 8;
   const int vpt = static_cast<int>((nvec + kQuantThreads - 1) / kQuantThreads);
   const dim3 grid(static_cast<unsigned>(M));
   if (vpt <= 1)
-    quant_act_kernel<OutT, 1><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
+    quant_act_kernel<OutT, 1><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   else if (vpt <= 2)
-    quant_act_kernel<OutT, 2><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
+    quant_act_kernel<OutT, 2><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   else if (vpt <= 3)
-    quant_act_kernel<OutT, 3><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
+    quant_act_kernel<OutT, 3><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   else if (vpt <= 4)
-    quant_act_kernel<OutT, 4><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
+    quant_act_kernel<OutT, 4><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   else if (vpt <= 6)
-    quant_act_kernel<OutT, 6><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
+    quant_act_kernel<OutT, 6><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   else if (vpt <= 8)
-    quant_act_kernel<OutT, 8><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
+    quant_act_kernel<OutT, 8><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   else if (vpt <= 12)
-    quant_act_kernel<OutT, 12><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
+    quant_act_kernel<OutT, 12><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   else if (vpt <= 16)
-    quant_act_kernel<OutT, 16><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
+    quant_act_kernel<OutT, 16><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   else
-    quant_act_long_kernel<OutT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1);
+    quant_act_long_kernel<OutT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   return cudaGetLastError();
 }
 
@@ -235,9 +248,12 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const float* __restri
 __global__ void __launch_bounds__(kQuantThreads) codes_s8_to_f16_kernel(const int8_t* __restrict__ qa,
                                                                         int64_t K,
                                                                         __half* __restrict__ out,
-                                                                        int* __restrict__ row_l1) {
+                                                                        int* __restrict__ row_l1,
+                                                                        int* __restrict__ zero,
+                                                                        int zero_words) {
   __shared__ int ired[4];
   const int64_t m = blockIdx.x;
+  clear_words(zero, zero_words);
   const int64_t n16 = K / 16;
   int l1 = 0;
   for (int64_t i = threadIdx.x; i < n16; i += kQuantThreads) {
@@ -266,12 +282,12 @@ __global__ void __launch_bounds__(kQuantThreads) codes_s8_to_f16_kernel(const in
 
 cudaError_t launch_quant_act_s8(const __half* x, int64_t M, int64_t K, int8_t* q, float* sa,
                                 cudaStream_t st) {
-  return launch_quant_act<int8_t>(x, M, K, q, sa, nullptr, st);
+  return launch_quant_act<int8_t>(x, M, K, q, sa, nullptr, nullptr, 0, st);
 }
 
 cudaError_t launch_quant_act_f16(const __half* x, int64_t M, int64_t K, __half* q, float* sa,
-                                 int* row_l1, cudaStream_t st) {
-  return launch_quant_act<__half>(x, M, K, q, sa, row_l1, st);
+                                 int* row_l1, int* zero, int zero_words, cudaStream_t st) {
+  return launch_quant_act<__half>(x, M, K, q, sa, row_l1, zero, zero_words, st);
 }
 
 cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int group_size, bool int4,
@@ -287,8 +303,9 @@ cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int group_
 }
 
 cudaError_t launch_codes_s8_to_f16(const int8_t* qa, int64_t M, int64_t K, __half* out,
-                                   int* row_l1, cudaStream_t st) {
-  codes_s8_to_f16_kernel<<<static_cast<unsigned>(M), kQuantThreads, 0, st>>>(qa, K, out, row_l1);
+                                   int* row_l1, int* zero, int zero_words, cudaStream_t st) {
+  codes_s8_to_f16_kernel<<<static_cast<unsigned>(M), kQuantThreads, 0, st>>>(qa, K, out, row_l1,
+                                                                              zero, zero_words);
   return cudaGetLastError();
 }
 
