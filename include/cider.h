@@ -83,6 +83,12 @@ int cider_version(void);
 cider_status_t cider_quantize_act(const void* x, int64_t M, int64_t K,
                                   int8_t* qa, float* sa, void* stream);
 
+/* As cider_quantize_act for bf16 activations (the README's roadmap, "auto
+ * dtype float16/bfloat16"): x bf16 [M, K] is widened to fp32 exactly, then
+ * quantized by the same steps. */
+cider_status_t cider_quantize_act_bf16(const void* x, int64_t M, int64_t K,
+                                       int8_t* qa, float* sa, void* stream);
+
 /* Symmetric min-max INT8 weight quantization (Cider README, "Notes": min-max
  * scales; "Quantization": per channel or per group).  s_w = max|W| / 127 per
  * row (group_size 0) or per group_size-element block (64 or 128),
@@ -129,6 +135,29 @@ cider_status_t cider_w4a8_linear(const void* x, int64_t M, int64_t N, int64_t K,
                                  const uint8_t* qw_packed, const float* sw,
                                  int granularity, int group_size, void* y,
                                  void* stream);
+
+/* The two linears for bf16 activations x bf16 [M, K]; everything else,
+ * including the fp16 output y, as cider_w8a8_linear / cider_w4a8_linear.
+ * The rows are always quantized by a separate kernel (scratch from the
+ * library's pool), for every M. */
+cider_status_t cider_w8a8_linear_bf16(const void* x, int64_t M, int64_t N, int64_t K,
+                                      const int8_t* qw, const float* sw,
+                                      int granularity, int group_size, void* y,
+                                      void* stream);
+cider_status_t cider_w4a8_linear_bf16(const void* x, int64_t M, int64_t N, int64_t K,
+                                      const uint8_t* qw_packed, const float* sw,
+                                      int granularity, int group_size, void* y,
+                                      void* stream);
+
+/* Import of INT4 weights stored offset-binary (each nibble u holds the value
+ * u - 8: the "Symmetric INT4 (zp=8)" form of the README's "Quantization"
+ * table) into this library's two's complement nibbles (value v stored as
+ * v & 0xF), nibble order unchanged: dst[i] = src[i] with 8 subtracted from
+ * each nibble value.  nbytes bytes, device pointers aligned to 16 bytes; dst
+ * may equal src.  Returns CIDER_ERR_INVALID_ARGUMENT for nbytes < 0 or NULL
+ * pointers, CIDER_ERR_MISALIGNED for unaligned pointers. */
+cider_status_t cider_int4_from_offset_binary(const uint8_t* src, uint8_t* dst,
+                                             int64_t nbytes, void* stream);
 
 /* The two linears with the activation already quantized (qa int8 [M, K],
  * sa fp32 [M], as produced by cider_quantize_act).  Several projections that

@@ -54,6 +54,10 @@ def _configure(lib):
     lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
     lib.oracle_f32_to_f16.restype = ctypes.c_uint16
     lib.oracle_quantize_act.argtypes = [p, i64, i64, p, p]
+    lib.oracle_quantize_act_bf16.argtypes = [p, i64, i64, p, p]
+    lib.oracle_int4_from_offset_binary.argtypes = [p, i64, p]
+    lib.oracle_linear_rows_bf16.argtypes = [p, i64, i64, p, p, i64, i64, i64, p, p, p]
+    lib.oracle_linear_rows_bf16.restype = ctypes.c_int
     lib.oracle_quantize_weight_int8.argtypes = [p, i64, i64, i64, p, p]
     lib.oracle_quantize_weight_int4.argtypes = [p, i64, i64, i64, p, p]
     lib.oracle_pack_int4.argtypes = [p, i64, i64, p]
@@ -99,6 +103,28 @@ def quantize_act(x_f16: np.ndarray):
     sa = np.empty((M,), np.float32)
     _load().oracle_quantize_act(_ptr(x), M, K, _ptr(qa), _ptr(sa))
     return qa, sa
+
+
+def quantize_act_bf16(x_bf16_bits: np.ndarray):
+    """The same for bf16 activations, given as their uint16 bit patterns
+    [M,K] (numpy has no bf16 type): each widens exactly to fp32 (the README's
+    roadmap, "auto dtype float16/bfloat16")."""
+    x = _c(x_bf16_bits, np.uint16)
+    M, K = x.shape
+    qa = np.empty((M, K), np.int8)
+    sa = np.empty((M,), np.float32)
+    _load().oracle_quantize_act_bf16(_ptr(x), M, K, _ptr(qa), _ptr(sa))
+    return qa, sa
+
+
+def int4_from_offset_binary(src: np.ndarray) -> np.ndarray:
+    """uint8 bytes of offset-binary INT4 (nibble u holds u - 8; README
+    "Quantization": "Symmetric INT4 (zp=8)") -> the two's complement packing
+    of the same values, nibble order unchanged."""
+    src = _c(src, np.uint8)
+    dst = np.empty_like(src)
+    _load().oracle_int4_from_offset_binary(_ptr(src), src.size, _ptr(dst))
+    return dst
 
 
 # ---------------------------------------------------------------- a2 / a4
@@ -187,13 +213,14 @@ def dequant_pg(acc: np.ndarray, sa: np.ndarray, sw: np.ndarray) -> np.ndarray:
 
 # ---------------------------------------------------------------- whole layer
 def linear(x_f16: np.ndarray, qw_values: np.ndarray, sw: np.ndarray,
-           group_size: int = 0, rows=None, threads: int = 1) -> np.ndarray:
+           group_size: int = 0, rows=None, threads: int = 1, bf16: bool = False) -> np.ndarray:
     """The whole layer, y fp16 [len(rows), N], for the given activation rows
     (default: all).  ``qw_values`` holds the integer weight values (INT8, or
-    INT4 values from :func:`unpack_int4`).  Rows are independent, so
-    ``threads > 1`` runs disjoint row ranges of the same single-threaded C code
-    concurrently (ctypes releases the GIL)."""
-    x = f16_bits(x_f16)
+    INT4 values from :func:`unpack_int4`).  With ``bf16`` the activations are
+    bf16 bit patterns (uint16 [M,K]).  Rows are independent, so ``threads > 1``
+    runs disjoint row ranges of the same single-threaded C code concurrently
+    (ctypes releases the GIL)."""
+    x = _c(x_f16, np.uint16) if bf16 else f16_bits(x_f16)
     M, K = x.shape
     qw = _c(qw_values, np.int8)
     N = qw.shape[0]
@@ -209,9 +236,9 @@ def linear(x_f16: np.ndarray, qw_values: np.ndarray, sw: np.ndarray,
         qa_s = np.empty((K,), np.int8)
         acc_s = np.empty((N * G,), np.int32)
         r0, r1 = int(r0), int(r1)
-        st = lib.oracle_linear_rows(_ptr(xs), K, N, _ptr(qw), _ptr(sw), group_size,
-                                    r0, r1, _ptr(qa_s), _ptr(acc_s),
-                                    _ptr(y) + r0 * N * 2)
+        fn = lib.oracle_linear_rows_bf16 if bf16 else lib.oracle_linear_rows
+        st = fn(_ptr(xs), K, N, _ptr(qw), _ptr(sw), group_size, r0, r1, _ptr(qa_s), _ptr(acc_s),
+                _ptr(y) + r0 * N * 2)
         if st != 0:
             raise OverflowError("integer accumulator does not fit in int32")
 

@@ -51,6 +51,14 @@ static uint16_t f32_to_f16_bits(float f) {
   return bits;
 }
 
+/* bf16 is the upper half of an IEEE binary32: widening appends 16 zero bits. */
+static float bf16_bits_to_f32(uint16_t bits) {
+  uint32_t w = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return f;
+}
+
 float oracle_f16_to_f32(uint16_t bits) { return f16_bits_to_f32(bits); }
 uint16_t oracle_f32_to_f16(float f) { return f32_to_f16_bits(f); }
 
@@ -70,21 +78,34 @@ static int quantize_value(float v, float scale, int qmin, int qmax) {
 }
 
 /* a1: per-token activation quantization (Cider README, "Metal kernel
- * pipeline" step quantize_per_token; "Quantization" row "Activations"). */
-void oracle_quantize_act(const uint16_t* x_f16, int64_t M, int64_t K,
-                         int8_t* qa, float* sa) {
+ * pipeline" step quantize_per_token; "Quantization" row "Activations").
+ * `widen` turns one stored activation into its exact fp32 value. */
+static void quantize_act_rows(const uint16_t* x, int64_t M, int64_t K,
+                              float (*widen)(uint16_t), int8_t* qa, float* sa) {
   for (int64_t m = 0; m < M; ++m) {
-    const uint16_t* row = x_f16 + m * K;
+    const uint16_t* row = x + m * K;
     float amax = 0.0f;
     for (int64_t k = 0; k < K; ++k) {
-      float a = fabsf(f16_bits_to_f32(row[k]));
+      float a = fabsf(widen(row[k]));
       if (a > amax) amax = a;
     }
     float s = block_scale(amax, 127.0f);
     sa[m] = s;
     for (int64_t k = 0; k < K; ++k)
-      qa[m * K + k] = (int8_t)quantize_value(f16_bits_to_f32(row[k]), s, -127, 127);
+      qa[m * K + k] = (int8_t)quantize_value(widen(row[k]), s, -127, 127);
   }
+}
+
+void oracle_quantize_act(const uint16_t* x_f16, int64_t M, int64_t K,
+                         int8_t* qa, float* sa) {
+  quantize_act_rows(x_f16, M, K, f16_bits_to_f32, qa, sa);
+}
+
+/* The same for bf16 activations (the README's roadmap: "auto dtype
+ * float16/bfloat16"). */
+void oracle_quantize_act_bf16(const uint16_t* x_bf16, int64_t M, int64_t K,
+                              int8_t* qa, float* sa) {
+  quantize_act_rows(x_bf16, M, K, bf16_bits_to_f32, qa, sa);
 }
 
 /* a2: symmetric weight quantization, per output channel (group_size = 0) or
@@ -136,6 +157,17 @@ void oracle_pack_int4(const int8_t* q, int64_t N, int64_t K, uint8_t* packed) {
 /* Nibble -> signed value: a 4-bit two's complement number t in [0,15] is t
  * when t < 8 and t - 16 otherwise. */
 static int nibble_value(unsigned t) { return (t < 8u) ? (int)t : (int)t - 16; }
+
+/* Offset-binary INT4 ("Symmetric INT4 (zp=8)", README "Quantization" table):
+ * nibble u in [0,15] holds the value u - 8.  Re-encode every byte's two
+ * values as two's complement nibbles, low nibble first as in the packing. */
+void oracle_int4_from_offset_binary(const uint8_t* src, int64_t nbytes, uint8_t* dst) {
+  for (int64_t i = 0; i < nbytes; ++i) {
+    int lo = (int)(src[i] & 0xFu) - 8;
+    int hi = (int)(src[i] >> 4) - 8;
+    dst[i] = (uint8_t)(((unsigned)lo & 0xFu) | (((unsigned)hi & 0xFu) << 4));
+  }
+}
 
 void oracle_unpack_int4(const uint8_t* packed, int64_t N, int64_t K, int8_t* q) {
   for (int64_t n = 0; n < N; ++n)
@@ -204,7 +236,7 @@ void oracle_dequant_pg(const int32_t* acc, const float* sa, const float* sw,
  * INT4 values after oracle_unpack_int4).  group_size = 0 -> per-channel.
  * y receives (m1 - m0) rows of N fp16 values.  acc_scratch must hold
  * N * G int32; qa_scratch K int8.  Returns the GEMM status. */
-int oracle_linear_rows(const uint16_t* x_f16, int64_t K, int64_t N,
+static int linear_rows(const uint16_t* x, float (*widen)(uint16_t), int64_t K, int64_t N,
                        const int8_t* qw, const float* sw, int64_t group_size,
                        int64_t m0, int64_t m1, int8_t* qa_scratch,
                        int32_t* acc_scratch, uint16_t* y) {
@@ -212,7 +244,7 @@ int oracle_linear_rows(const uint16_t* x_f16, int64_t K, int64_t N,
   int status = 0;
   for (int64_t m = m0; m < m1; ++m) {
     float sa;
-    oracle_quantize_act(x_f16 + m * K, 1, K, qa_scratch, &sa);
+    quantize_act_rows(x + m * K, 1, K, widen, qa_scratch, &sa);
     if (oracle_gemm_acc(qa_scratch, qw, 1, N, K, group_size, acc_scratch) != 0)
       status = -1;
     uint16_t* yrow = y + (m - m0) * N;
@@ -222,4 +254,20 @@ int oracle_linear_rows(const uint16_t* x_f16, int64_t K, int64_t N,
       oracle_dequant_pc(acc_scratch, &sa, sw, 1, N, yrow);
   }
   return status;
+}
+
+int oracle_linear_rows(const uint16_t* x_f16, int64_t K, int64_t N,
+                       const int8_t* qw, const float* sw, int64_t group_size,
+                       int64_t m0, int64_t m1, int8_t* qa_scratch,
+                       int32_t* acc_scratch, uint16_t* y) {
+  return linear_rows(x_f16, f16_bits_to_f32, K, N, qw, sw, group_size, m0, m1, qa_scratch,
+                     acc_scratch, y);
+}
+
+int oracle_linear_rows_bf16(const uint16_t* x_bf16, int64_t K, int64_t N,
+                            const int8_t* qw, const float* sw, int64_t group_size,
+                            int64_t m0, int64_t m1, int8_t* qa_scratch,
+                            int32_t* acc_scratch, uint16_t* y) {
+  return linear_rows(x_bf16, bf16_bits_to_f32, K, N, qw, sw, group_size, m0, m1, qa_scratch,
+                     acc_scratch, y);
 }

@@ -4,7 +4,7 @@
  * and the benchmark's CPU-baseline leg, never by the product library.
  *
  * All arrays are dense row-major host memory owned by the caller.
- * fp16 values travel as their uint16_t bit patterns.
+ * fp16 and bf16 values travel as their uint16_t bit patterns.
  */
 #ifndef CIDER_ORACLE_H
 #define CIDER_ORACLE_H
@@ -21,6 +21,9 @@ uint16_t oracle_f32_to_f16(float f);
 /* x_f16 [M,K] -> qa int8 [M,K], sa fp32 [M] */
 void oracle_quantize_act(const uint16_t* x_f16, int64_t M, int64_t K,
                          int8_t* qa, float* sa);
+/* the same from x_bf16 [M,K] */
+void oracle_quantize_act_bf16(const uint16_t* x_bf16, int64_t M, int64_t K,
+                              int8_t* qa, float* sa);
 
 /* W fp32 [N,K] -> qw int8 [N,K], sw fp32 [N, G] (G = 1 when group_size = 0) */
 void oracle_quantize_weight_int8(const float* W, int64_t N, int64_t K,
@@ -32,6 +35,8 @@ void oracle_quantize_weight_int4(const float* W, int64_t N, int64_t K,
 /* q int8 [N,K] with values in [-8,7] <-> packed uint8 [N, K/2] */
 void oracle_pack_int4(const int8_t* q, int64_t N, int64_t K, uint8_t* packed);
 void oracle_unpack_int4(const uint8_t* packed, int64_t N, int64_t K, int8_t* q);
+/* offset-binary INT4 bytes (nibble u = value + 8) -> two's complement bytes */
+void oracle_int4_from_offset_binary(const uint8_t* src, int64_t nbytes, uint8_t* dst);
 
 /* acc int32 [M, N, G]; returns 0, or -1 if some sum overflows int32 */
 int oracle_gemm_acc(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N,
@@ -49,6 +54,11 @@ int oracle_linear_rows(const uint16_t* x_f16, int64_t K, int64_t N,
                        const int8_t* qw, const float* sw, int64_t group_size,
                        int64_t m0, int64_t m1, int8_t* qa_scratch,
                        int32_t* acc_scratch, uint16_t* y);
+/* the same with x_bf16 */
+int oracle_linear_rows_bf16(const uint16_t* x_bf16, int64_t K, int64_t N,
+                            const int8_t* qw, const float* sw, int64_t group_size,
+                            int64_t m0, int64_t m1, int8_t* qa_scratch,
+                            int32_t* acc_scratch, uint16_t* y);
 
 #ifdef __cplusplus
 }

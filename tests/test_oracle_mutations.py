@@ -34,7 +34,12 @@ MUTATIONS = [
     ("pg_reversed_order", "for (int64_t g = 0; g < G; ++g) {\n        float scale",
      "for (int64_t g = G - 1; g >= 0; --g) {\n        float scale"),
     ("pc_dropped_weight_scale", "v = v * sw[n];", "v = v * 1.0f;"),
-    ("act_amax_signed", "float a = fabsf(f16_bits_to_f32(row[k]));", "float a = f16_bits_to_f32(row[k]);"),
+    ("act_amax_signed", "float a = fabsf(widen(row[k]));", "float a = widen(row[k]);"),
+    ("bf16_widen_shift", "uint32_t w = (uint32_t)bits << 16;", "uint32_t w = (uint32_t)bits << 15;"),
+    ("bf16_read_as_fp16", "quantize_act_rows(x_bf16, M, K, bf16_bits_to_f32, qa, sa);",
+     "quantize_act_rows(x_bf16, M, K, f16_bits_to_f32, qa, sa);"),
+    ("offset_zero_point_7", "int lo = (int)(src[i] & 0xFu) - 8;", "int lo = (int)(src[i] & 0xFu) - 7;"),
+    ("offset_high_nibble_kept", "int hi = (int)(src[i] >> 4) - 8;", "int hi = nibble_value(src[i] >> 4);"),
 ]
 
 PIN_TESTS = [
@@ -55,6 +60,11 @@ PIN_TESTS = [
     pins.test_dequant_pc_exact_emulation,
     pins.test_dequant_pg_order_hand_worked,
     pins.test_dequant_pg_exact_emulation,
+    pins.test_quantize_act_bf16_hand_worked_cases,
+    lambda: pins.test_quantize_act_bf16_brute_force_all_bf16_below_amax(0x4049),
+    pins.test_quantize_act_bf16_agrees_with_fp16_on_shared_values,
+    pins.test_int4_offset_binary_hand_worked,
+    pins.test_int4_offset_binary_exhaustive,
 ]
 
 

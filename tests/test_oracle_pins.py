@@ -345,3 +345,101 @@ def test_linear_close_to_unquantized_product():
         y = oracle.linear(x, qw, sw, gs).astype(np.float64)
         cos = (y * ref).sum() / np.sqrt((y * y).sum() * (ref * ref).sum())
         assert cos > (0.99 if bits == 8 else 0.95), (bits, gs, cos)
+
+
+# ------------------------------------------------------------ a1 with bf16 activations
+def _bf16_to_f32(bits):
+    """bf16 bit patterns -> fp32 values, by definition (the upper half of an
+    IEEE binary32)."""
+    return (np.asarray(bits, np.uint32) << 16).view(np.float32)
+
+
+def test_bf16_widening_matches_torch_for_every_pattern():
+    """The oracle's bf16 reading of every bit pattern equals PyTorch's own
+    bf16 -> fp32 conversion (a library routine independent of the oracle):
+    a row holding one pattern at a time quantizes against amax = |x|."""
+    import torch
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    np.testing.assert_array_equal(_bf16_to_f32(bits)[np.isfinite(ref)], ref[np.isfinite(ref)])
+    finite = bits[np.isfinite(ref) & (np.abs(ref) > 0)]
+    qa, sa = oracle.quantize_act_bf16(finite[:, None])
+    np.testing.assert_array_equal(sa, _f32_div(np.abs(ref[np.isfinite(ref) & (np.abs(ref) > 0)]), 127))
+    assert np.all(np.abs(qa[:, 0]) == 127)
+
+
+def test_quantize_act_bf16_hand_worked_cases():
+    for case in _blocks(os.path.join(GOLDEN, "quant_act_bf16_hand.txt"), ("x", "q", "s")):
+        x = np.array([int(v, 16) for v in case["x"]], np.uint16)[None, :]
+        qa, sa = oracle.quantize_act_bf16(x)
+        assert qa[0].tolist() == [int(v) for v in case["q"]], case
+        assert sa[0] == np.float32(float.fromhex(case["s"][0])), case
+
+
+@pytest.mark.parametrize("amax_bits", [0x3F80, 0x42FE, 0x4049, 0x7F7F, 0x0080, 0x007F, 0x3A83])
+def test_quantize_act_bf16_brute_force_all_bf16_below_amax(amax_bits):
+    """Every finite bf16 value with |x| <= amax (1, 127, 3.140625, the largest
+    finite, the smallest normal, a subnormal, ~0.001), in rows that contain
+    amax, against an independent binary64 computation of the same steps."""
+    amax = float(_bf16_to_f32([amax_bits])[0])
+    allb = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    allv = _bf16_to_f32(allb)
+    with np.errstate(invalid="ignore"):
+        ok = np.isfinite(allv) & (np.abs(allv.astype(np.float64)) <= amax)
+    vals = allb[ok]
+    W = 1024
+    pad = (-len(vals)) % (W - 1)
+    vals = np.concatenate([vals, np.zeros(pad, np.uint16)]).reshape(-1, W - 1)
+    x = np.concatenate([np.full((vals.shape[0], 1), amax_bits, np.uint16), vals], axis=1)
+    qa, sa = oracle.quantize_act_bf16(x)
+    for r in range(x.shape[0]):
+        xf = _bf16_to_f32(x[r]).astype(np.float64)
+        s = _f32_div(np.max(np.abs(xf)), 127)
+        q = np.clip(np.rint(_f32_div(xf, s).astype(np.float64)), -127, 127).astype(np.int8)
+        assert sa[r] == s
+        np.testing.assert_array_equal(qa[r], q)
+
+
+def test_quantize_act_bf16_agrees_with_fp16_on_shared_values():
+    """Values exact in both formats quantize identically from either."""
+    rng = np.random.default_rng(21)
+    ints = rng.integers(-255, 256, size=(9, 200))
+    x = (ints * np.float32(2.0) ** rng.integers(-8, 3, size=(9, 1))).astype(np.float32)
+    x16 = x.astype(np.float16)
+    assert np.array_equal(x16.astype(np.float32), x)
+    xb = (x.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(_bf16_to_f32(xb), x)
+    q1, s1 = oracle.quantize_act(x16)
+    q2, s2 = oracle.quantize_act_bf16(xb)
+    np.testing.assert_array_equal(q1, q2)
+    np.testing.assert_array_equal(s1, s2)
+
+
+def test_linear_bf16_is_composition():
+    rng = np.random.default_rng(22)
+    xb = (rng.standard_normal((5, 256)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    qw = rng.integers(-127, 128, size=(24, 256)).astype(np.int8)
+    sw = rng.random(24).astype(np.float32) * 0.01
+    y = oracle.linear(xb, qw, sw, 0, bf16=True)
+    qa, sa = oracle.quantize_act_bf16(xb)
+    np.testing.assert_array_equal(y.view(np.uint16),
+                                  oracle.dequant_pc(oracle.gemm_acc(qa, qw, 0)[:, :, 0], sa, sw).view(np.uint16))
+
+
+# ------------------------------------------------------------ offset-binary INT4 import
+def test_int4_offset_binary_hand_worked():
+    """"Symmetric INT4 (zp=8)" ("Quantization" table): nibble u holds u - 8.
+    0x00 -> (-8, -8) -> 0x88; 0x88 -> (0, 0) -> 0x00; 0xFF -> (7, 7) -> 0x77;
+    0x80 -> (-8, 0) -> 0x08; 0x08 -> (0, -8) -> 0x80; 0x9A -> (2, 1) -> 0x12."""
+    src = np.array([0x00, 0x88, 0xFF, 0x80, 0x08, 0x9A], np.uint8)
+    assert oracle.int4_from_offset_binary(src).tolist() == [0x88, 0x00, 0x77, 0x08, 0x80, 0x12]
+
+
+def test_int4_offset_binary_exhaustive():
+    """All 256 bytes: the re-encoded nibbles decode (two's complement, low
+    nibble first) to the offset values u - 8."""
+    src = np.arange(256, dtype=np.uint8)
+    dst = oracle.int4_from_offset_binary(src)
+    vals = oracle.unpack_int4(dst[None, :])[0].astype(np.int16)
+    np.testing.assert_array_equal(vals[0::2], (src & 0xF).astype(np.int16) - 8)
+    np.testing.assert_array_equal(vals[1::2], (src >> 4).astype(np.int16) - 8)

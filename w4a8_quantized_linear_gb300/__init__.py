@@ -46,10 +46,14 @@ def _declare(lib):
         "cider_status_string": ([i32], ctypes.c_char_p),
         "cider_version": ([], i32),
         "cider_quantize_act": ([p, i64, i64, p, p, p], i32),
+        "cider_quantize_act_bf16": ([p, i64, i64, p, p, p], i32),
+        "cider_int4_from_offset_binary": ([p, p, i64, p], i32),
         "cider_quantize_weight_int8": ([p, i64, i64, i32, p, p, p], i32),
         "cider_quantize_weight_int4": ([p, i64, i64, i32, p, p, p], i32),
         "cider_w8a8_linear": ([p, i64, i64, i64, p, p, i32, i32, p, p], i32),
         "cider_w4a8_linear": ([p, i64, i64, i64, p, p, i32, i32, p, p], i32),
+        "cider_w8a8_linear_bf16": ([p, i64, i64, i64, p, p, i32, i32, p, p], i32),
+        "cider_w4a8_linear_bf16": ([p, i64, i64, i64, p, p, i32, i32, p, p], i32),
         "cider_w8a8_linear_prequant": ([p, p, i64, i64, i64, p, p, i32, i32, p, p], i32),
         "cider_w4a8_linear_prequant": ([p, p, i64, i64, i64, p, p, i32, i32, p, p], i32),
         "cider_w8a8_accumulators": ([p, i64, i64, i64, p, i32, p, p], i32),
@@ -115,15 +119,37 @@ def cider_is_available() -> bool:
     return bool(_load().cider_is_available())
 
 
-def cider_quantize_act(x: torch.Tensor):
-    """x fp16 [M, K] -> (qa int8 [M, K], sa fp32 [M])."""
-    _need(x, torch.float16, "x", 2)
+def _quantize_act(fn, x, dtype):
+    _need(x, dtype, "x", 2)
     M, K = x.shape
     qa = torch.empty((M, K), dtype=torch.int8, device=x.device)
     sa = torch.empty((M,), dtype=torch.float32, device=x.device)
-    _check("cider_quantize_act",
-           _load().cider_quantize_act(_ptr(x), M, K, _ptr(qa), _ptr(sa), _stream(x)))
+    _check(fn, getattr(_load(), fn)(_ptr(x), M, K, _ptr(qa), _ptr(sa), _stream(x)))
     return qa, sa
+
+
+def cider_quantize_act(x: torch.Tensor):
+    """x fp16 [M, K] -> (qa int8 [M, K], sa fp32 [M])."""
+    return _quantize_act("cider_quantize_act", x, torch.float16)
+
+
+def cider_quantize_act_bf16(x: torch.Tensor):
+    """x bf16 [M, K] -> (qa int8 [M, K], sa fp32 [M])."""
+    return _quantize_act("cider_quantize_act_bf16", x, torch.bfloat16)
+
+
+def cider_int4_from_offset_binary(packed: torch.Tensor, out=None):
+    """uint8 INT4 bytes stored offset-binary (nibble u = value + 8) -> the
+    library's two's complement packing (out may be packed itself)."""
+    if not isinstance(packed, torch.Tensor) or not packed.is_cuda or packed.dtype != torch.uint8:
+        raise TypeError("packed must be a CUDA uint8 tensor")
+    if not packed.is_contiguous():
+        raise ValueError("packed must be contiguous")
+    dst = out if out is not None else torch.empty_like(packed)
+    _check("cider_int4_from_offset_binary",
+           _load().cider_int4_from_offset_binary(_ptr(packed), _ptr(dst), packed.numel(),
+                                                 _stream(packed)))
+    return dst
 
 
 def cider_quantize_weight_int8(w: torch.Tensor, group_size: int = 0):
@@ -156,8 +182,8 @@ def _gran(group_size: int) -> int:
     return CIDER_PER_GROUP if group_size else CIDER_PER_CHANNEL
 
 
-def _linear(fn, x, qw, sw, group_size, int4, out=None):
-    _need(x, torch.float16, "x", 2)
+def _linear(fn, x, qw, sw, group_size, int4, out=None, x_dtype=torch.float16):
+    _need(x, x_dtype, "x", 2)
     _need(qw, torch.uint8 if int4 else torch.int8, "qw", 2)
     M, K = x.shape
     N = qw.shape[0]
@@ -180,6 +206,17 @@ def cider_w8a8_linear(x, qw, sw, group_size: int = 0, out=None):
 def cider_w4a8_linear(x, qw_packed, sw, group_size: int = 0, out=None):
     """W4A8 linear with qw_packed uint8 [N, K/2]."""
     return _linear("cider_w4a8_linear", x, qw_packed, sw, group_size, True, out)
+
+
+def cider_w8a8_linear_bf16(x, qw, sw, group_size: int = 0, out=None):
+    """As cider_w8a8_linear for x bf16 [M, K]; y is fp16."""
+    return _linear("cider_w8a8_linear_bf16", x, qw, sw, group_size, False, out, torch.bfloat16)
+
+
+def cider_w4a8_linear_bf16(x, qw_packed, sw, group_size: int = 0, out=None):
+    """As cider_w4a8_linear for x bf16 [M, K]; y is fp16."""
+    return _linear("cider_w4a8_linear_bf16", x, qw_packed, sw, group_size, True, out,
+                   torch.bfloat16)
 
 
 def _linear_prequant(fn, qa, sa, qw, sw, group_size, int4, out=None):

@@ -170,7 +170,8 @@ cudaError_t timed_launch(cudaStream_t st, F&& launch) {
 }
 
 struct LinearArgs {
-  const void* x = nullptr;  // fp16 activations (or null for the prequant forms)
+  const void* x = nullptr;  // fp16 / bf16 activations (or null for the prequant forms)
+  bool x_bf16 = false;
   const int8_t* qa = nullptr;
   const float* sa = nullptr;
   int64_t M = 0, N = 0, K = 0;
@@ -223,16 +224,19 @@ cider_status_t run_linear(const LinearArgs& a) {
     // small M: for one token or short rows the GEMV quantizes the rows itself
     // (every CTA repeats that work, cheaper than a second launch for so few
     // values); otherwise one quantization kernel writes the int8 codes first.
+    // bf16 rows always go through the quantization kernel (the GEMV stages fp16).
     const __half* xg = static_cast<const __half*>(a.x);
     const int8_t* qa = a.qa;
     const float* sa = a.sa;
-    if (xg && !cider::gemv_quantizes_itself(a.M, a.K)) {
+    if (a.x && (a.x_bf16 || !cider::gemv_quantizes_itself(a.M, a.K))) {
       const size_t qbytes = round_up(static_cast<size_t>(a.M * a.K), 256);
       cudaError_t e = scratch_alloc(scratch, dev, qbytes + round_up(4 * a.M, 256), a.st);
       if (e != cudaSuccess) return cuda_status(e);
       int8_t* qs = static_cast<int8_t*>(scratch.ptr);
       float* ss = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch.ptr) + qbytes);
-      e = cider::launch_quant_act_s8(xg, a.M, a.K, qs, ss, a.st);
+      e = a.x_bf16 ? cider::launch_quant_act_s8_bf16(static_cast<const __nv_bfloat16*>(a.x), a.M,
+                                                     a.K, qs, ss, a.st)
+                   : cider::launch_quant_act_s8(xg, a.M, a.K, qs, ss, a.st);
       if (e != cudaSuccess) return cuda_status(e);
       xg = nullptr;
       qa = qs;
@@ -257,8 +261,11 @@ cider_status_t run_linear(const LinearArgs& a) {
   const float* sa = a.sa;
   if (a.x) {
     float* sscr = reinterpret_cast<float*>(sbase + qbytes);
-    e = cider::launch_quant_act_f16(static_cast<const __half*>(a.x), a.M, a.K, q16, sscr, row_l1,
-                                    zero, gsc.zero_words, a.st);
+    e = a.x_bf16 ? cider::launch_quant_act_f16_from_bf16(static_cast<const __nv_bfloat16*>(a.x),
+                                                         a.M, a.K, q16, sscr, row_l1, zero,
+                                                         gsc.zero_words, a.st)
+                 : cider::launch_quant_act_f16(static_cast<const __half*>(a.x), a.M, a.K, q16, sscr,
+                                               row_l1, zero, gsc.zero_words, a.st);
     sa = sscr;
   } else {
     e = cider::launch_codes_s8_to_f16(a.qa, a.M, a.K, q16, row_l1, zero, gsc.zero_words, a.st);
@@ -314,8 +321,8 @@ const char* cider_status_string(int status) {
   }
 }
 
-cider_status_t cider_quantize_act(const void* x, int64_t M, int64_t K, int8_t* qa, float* sa,
-                                  void* stream) {
+static cider_status_t quantize_act_entry(const void* x, bool bf16, int64_t M, int64_t K, int8_t* qa,
+                                         float* sa, void* stream) {
   return guarded([&]() -> cider_status_t {
     if (M == 0) return CIDER_OK;
     if (M < 0 || M > kMaxDim || !x || !qa || !sa || !valid_k(K)) return CIDER_ERR_INVALID_ARGUMENT;
@@ -323,8 +330,34 @@ cider_status_t cider_quantize_act(const void* x, int64_t M, int64_t K, int8_t* q
     if (!aligned(sa, 4)) return CIDER_ERR_MISALIGNED;
     cider_status_t s = check_device(nullptr, nullptr);
     if (s != CIDER_OK) return s;
-    return cuda_status(cider::launch_quant_act_s8(static_cast<const __half*>(x), M, K, qa, sa,
-                                                  static_cast<cudaStream_t>(stream)));
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return cuda_status(bf16 ? cider::launch_quant_act_s8_bf16(static_cast<const __nv_bfloat16*>(x),
+                                                              M, K, qa, sa, st)
+                            : cider::launch_quant_act_s8(static_cast<const __half*>(x), M, K, qa,
+                                                         sa, st));
+  });
+}
+
+cider_status_t cider_quantize_act(const void* x, int64_t M, int64_t K, int8_t* qa, float* sa,
+                                  void* stream) {
+  return quantize_act_entry(x, false, M, K, qa, sa, stream);
+}
+
+cider_status_t cider_quantize_act_bf16(const void* x, int64_t M, int64_t K, int8_t* qa, float* sa,
+                                       void* stream) {
+  return quantize_act_entry(x, true, M, K, qa, sa, stream);
+}
+
+cider_status_t cider_int4_from_offset_binary(const uint8_t* src, uint8_t* dst, int64_t nbytes,
+                                             void* stream) {
+  return guarded([&]() -> cider_status_t {
+    if (nbytes == 0) return CIDER_OK;
+    if (nbytes < 0 || !src || !dst) return CIDER_ERR_INVALID_ARGUMENT;
+    if (!aligned(src, 16) || !aligned(dst, 16)) return CIDER_ERR_MISALIGNED;
+    cider_status_t s = check_device(nullptr, nullptr);
+    if (s != CIDER_OK) return s;
+    return cuda_status(
+        cider::launch_int4_from_offset(src, dst, nbytes, static_cast<cudaStream_t>(stream)));
   });
 }
 
@@ -340,10 +373,12 @@ cider_status_t cider_quantize_weight_int4(const float* w, int64_t N, int64_t K, 
 
 static cider_status_t linear_entry(const void* x, const int8_t* qa, const float* sa, int64_t M,
                                    int64_t N, int64_t K, const void* w, bool int4, const float* sw,
-                                   int granularity, int group_size, void* y, void* stream) {
+                                   int granularity, int group_size, void* y, void* stream,
+                                   bool x_bf16 = false) {
   return guarded([&] {
     LinearArgs a;
     a.x = x;
+    a.x_bf16 = x_bf16;
     a.qa = qa;
     a.sa = sa;
     a.M = M;
@@ -376,6 +411,22 @@ cider_status_t cider_w4a8_linear(const void* x, int64_t M, int64_t N, int64_t K,
   if (x == nullptr && M != 0 && N != 0) return CIDER_ERR_INVALID_ARGUMENT;
   return linear_entry(x, nullptr, nullptr, M, N, K, qw_packed, true, sw, granularity, group_size, y,
                       stream);
+}
+
+cider_status_t cider_w8a8_linear_bf16(const void* x, int64_t M, int64_t N, int64_t K,
+                                      const int8_t* qw, const float* sw, int granularity,
+                                      int group_size, void* y, void* stream) {
+  if (x == nullptr && M != 0 && N != 0) return CIDER_ERR_INVALID_ARGUMENT;
+  return linear_entry(x, nullptr, nullptr, M, N, K, qw, false, sw, granularity, group_size, y,
+                      stream, true);
+}
+
+cider_status_t cider_w4a8_linear_bf16(const void* x, int64_t M, int64_t N, int64_t K,
+                                      const uint8_t* qw_packed, const float* sw, int granularity,
+                                      int group_size, void* y, void* stream) {
+  if (x == nullptr && M != 0 && N != 0) return CIDER_ERR_INVALID_ARGUMENT;
+  return linear_entry(x, nullptr, nullptr, M, N, K, qw_packed, true, sw, granularity, group_size, y,
+                      stream, true);
 }
 
 cider_status_t cider_w8a8_linear_prequant(const int8_t* qa, const float* sa, int64_t M, int64_t N,

@@ -2,6 +2,7 @@
 // library (not part of the public ABI).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -46,8 +47,17 @@ cudaError_t launch_quant_act_s8(const __half* x, int64_t M, int64_t K, int8_t* q
 // clears `zero_words` int32 words at `zero` (the GEMM's flags) on the way.
 cudaError_t launch_quant_act_f16(const __half* x, int64_t M, int64_t K, __half* q, float* sa,
                                  int* row_l1, int* zero, int zero_words, cudaStream_t st);
+// The same two from bf16 activations.
+cudaError_t launch_quant_act_s8_bf16(const __nv_bfloat16* x, int64_t M, int64_t K, int8_t* q,
+                                     float* sa, cudaStream_t st);
+cudaError_t launch_quant_act_f16_from_bf16(const __nv_bfloat16* x, int64_t M, int64_t K, __half* q,
+                                           float* sa, int* row_l1, int* zero, int zero_words,
+                                           cudaStream_t st);
 cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int group_size, bool int4,
                                 uint8_t* q, float* sw, cudaStream_t st);
+// Offset-binary INT4 bytes -> two's complement INT4 bytes (src may equal dst).
+cudaError_t launch_int4_from_offset(const uint8_t* src, uint8_t* dst, int64_t nbytes,
+                                    cudaStream_t st);
 cudaError_t launch_codes_s8_to_f16(const int8_t* qa, int64_t M, int64_t K, __half* out,
                                    int* row_l1, int* zero, int zero_words, cudaStream_t st);
 

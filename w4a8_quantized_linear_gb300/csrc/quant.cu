@@ -8,8 +8,13 @@
 //   q   = clamp(rint(x / s_a), -127, 127) with ties to even.
 // Weight quantization follows "Notes" (min-max scales) and the "Quantization"
 // table (INT8 per channel or per group of 64 / 128; INT4 for W4A8, "Modes").
+// Activations may be fp16 or bf16 (the "auto dtype float16/bfloat16" item of
+// the README's roadmap); both widen to fp32 exactly before the same steps.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "cider_device.cuh"
 #include "cider_internal.h"
@@ -34,13 +39,51 @@ __device__ __forceinline__ float block_max_128(float v, float* red) {
   return v;
 }
 
-__device__ __forceinline__ float quant_code(float x, float s, float r) { return act_code(x, s, r); }
+// Code of x for scale s.  fp16 rows use the reciprocal-based correctly rounded
+// quotient of act_code (its conditions hold on the fp16 range); bf16 rows
+// reach scales down to ~2^-140, where 1/s overflows, so they divide.
+template <typename InT>
+__device__ __forceinline__ float quant_code(float x, float s, float r) {
+  if constexpr (std::is_same<InT, __half>::value) return act_code(x, s, r);
+  const float q = rintf(__fdiv_rn(x, s));
+  return fminf(fmaxf(q, -127.0f), 127.0f);
+}
 
-// Eight fp16 values -> eight codes, stored as int8 (8 bytes) or as fp16
+// Two packed 16-bit activations -> two fp32 values (exact widening).
+template <typename InT>
+__device__ __forceinline__ float2 widen2(uint32_t w);
+template <>
+__device__ __forceinline__ float2 widen2<__half>(uint32_t w) {
+  __half2 h;
+  memcpy(&h, &w, 4);
+  return __half22float2(h);
+}
+template <>
+__device__ __forceinline__ float2 widen2<__nv_bfloat16>(uint32_t w) {
+  __nv_bfloat162 h;
+  memcpy(&h, &w, 4);
+  return __bfloat1622float2(h);
+}
+
+// max |v| over eight packed activations
+template <typename InT>
+__device__ __forceinline__ float amax8(const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float a = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 f = widen2<InT>(w[j]);
+    a = fmaxf(a, fmaxf(fabsf(f.x), fabsf(f.y)));
+  }
+  return a;
+}
+
+// Eight activations -> eight codes, stored as int8 (8 bytes) or as fp16
 // integers (16 bytes; exact, the operand format of the tensor-core GEMM).
+template <typename InT>
 __device__ __forceinline__ int store_codes(int8_t* q, int64_t off, const uint4& v, float s,
                                            float r) {
-  const __half2* h = reinterpret_cast<const __half2*>(&v);
+  const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
   uint32_t w[2];
   int l1 = 0;
 #pragma unroll
@@ -48,9 +91,9 @@ __device__ __forceinline__ int store_codes(int8_t* q, int64_t off, const uint4& 
     uint32_t b = 0;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      float2 f = __half22float2(h[2 * j + e]);
-      int c0 = static_cast<int>(quant_code(f.x, s, r));
-      int c1 = static_cast<int>(quant_code(f.y, s, r));
+      float2 f = widen2<InT>(vw[2 * j + e]);
+      int c0 = static_cast<int>(quant_code<InT>(f.x, s, r));
+      int c1 = static_cast<int>(quant_code<InT>(f.y, s, r));
       l1 += abs(c0) + abs(c1);
       b |= (static_cast<uint32_t>(c0 & 0xFF) << (16 * e)) |
            (static_cast<uint32_t>(c1 & 0xFF) << (16 * e + 8));
@@ -60,16 +103,17 @@ __device__ __forceinline__ int store_codes(int8_t* q, int64_t off, const uint4& 
   *reinterpret_cast<uint2*>(q + off) = make_uint2(w[0], w[1]);
   return l1;
 }
+template <typename InT>
 __device__ __forceinline__ int store_codes(__half* q, int64_t off, const uint4& v, float s,
                                            float r) {
-  const __half2* h = reinterpret_cast<const __half2*>(&v);
+  const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
   uint4 o;
   uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
   float l1 = 0.0f;  // a sum of at most 8 codes: exact
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    float2 f = __half22float2(h[j]);
-    const float c0 = quant_code(f.x, s, r), c1 = quant_code(f.y, s, r);
+    float2 f = widen2<InT>(vw[j]);
+    const float c0 = quant_code<InT>(f.x, s, r), c1 = quant_code<InT>(f.y, s, r);
     l1 += fabsf(c0) + fabsf(c1);
     __half2 r = __floats2half2_rn(c0, c1);
     ow[j] = *reinterpret_cast<uint32_t*>(&r);
@@ -96,8 +140,8 @@ __device__ __forceinline__ void clear_words(int* zero, int n) {
 
 // One CTA of 128 threads per row; the row stays in registers between the
 // amax pass and the quantization pass (VPT 16-byte vectors per thread).
-template <typename OutT, int VPT>
-__global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const __half* __restrict__ x,
+template <typename OutT, int VPT, typename InT>
+__global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const InT* __restrict__ x,
                                                                   int64_t K, OutT* __restrict__ q,
                                                                   float* __restrict__ sa,
                                                                   int* __restrict__ row_l1,
@@ -110,18 +154,15 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const __half* 
   const uint4* row = reinterpret_cast<const uint4*>(x + m * K);
   const int nvec = static_cast<int>(K >> 3);
   uint4 v[VPT];
-  __half2 amax2 = __float2half2_rn(0.0f);
+  float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int idx = threadIdx.x + i * kQuantThreads;
     if (idx < nvec) {
       v[i] = ld_stream_v4(row + idx);
-      const __half2* h = reinterpret_cast<const __half2*>(&v[i]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) amax2 = __hmax2(amax2, __habs2(h[j]));
+      amax = fmaxf(amax, amax8<InT>(v[i]));
     }
   }
-  float amax = fmaxf(__low2float(amax2), __high2float(amax2));
   amax = block_max_128(amax, red);
   const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
   const float r = __frcp_rn(s);
@@ -130,7 +171,7 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const __half* 
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int idx = threadIdx.x + i * kQuantThreads;
-    if (idx < nvec) l1 += store_codes(q, m * K + static_cast<int64_t>(idx) * 8, v[i], s, r);
+    if (idx < nvec) l1 += store_codes<InT>(q, m * K + static_cast<int64_t>(idx) * 8, v[i], s, r);
   }
   if (row_l1 != nullptr) {
     l1 = block_sum_128(l1, ired);
@@ -140,8 +181,8 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const __half* 
 
 // Rows longer than the register-resident variants: two passes over global
 // memory (the second pass hits L1/L2).
-template <typename OutT>
-__global__ void __launch_bounds__(kQuantThreads) quant_act_long_kernel(const __half* __restrict__ x,
+template <typename OutT, typename InT>
+__global__ void __launch_bounds__(kQuantThreads) quant_act_long_kernel(const InT* __restrict__ x,
                                                                        int64_t K,
                                                                        OutT* __restrict__ q,
                                                                        float* __restrict__ sa,
@@ -154,51 +195,45 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_long_kernel(const __h
   clear_words(zero, zero_words);
   const uint4* row = reinterpret_cast<const uint4*>(x + m * K);
   const int64_t nvec = K >> 3;
-  __half2 amax2 = __float2half2_rn(0.0f);
-  for (int64_t idx = threadIdx.x; idx < nvec; idx += kQuantThreads) {
-    uint4 v = row[idx];
-    const __half2* h = reinterpret_cast<const __half2*>(&v);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) amax2 = __hmax2(amax2, __habs2(h[j]));
-  }
-  float amax = fmaxf(__low2float(amax2), __high2float(amax2));
+  float amax = 0.0f;
+  for (int64_t idx = threadIdx.x; idx < nvec; idx += kQuantThreads) amax = fmaxf(amax, amax8<InT>(row[idx]));
   amax = block_max_128(amax, red);
   const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
   const float r = __frcp_rn(s);
   if (threadIdx.x == 0) sa[m] = s;
   int l1 = 0;
   for (int64_t idx = threadIdx.x; idx < nvec; idx += kQuantThreads)
-    l1 += store_codes(q, m * K + idx * 8, row[idx], s, r);
+    l1 += store_codes<InT>(q, m * K + idx * 8, row[idx], s, r);
   if (row_l1 != nullptr) {
     l1 = block_sum_128(l1, ired);
     if (threadIdx.x == 0) row_l1[m] = l1;
   }
 }
 
-template <typename OutT>
-cudaError_t launch_quant_act(const __half* x, int64_t M, int64_t K, OutT* q, float* sa,
+template <typename OutT, typename InT>
+cudaError_t launch_quant_act(const InT* x, int64_t M, int64_t K, OutT* q, float* sa,
                              int* row_l1, int* zero, int zero_words, cudaStream_t st) {
   const int64_t nvec = K / 8;
   const int vpt = static_cast<int>((nvec + kQuantThreads - 1) / kQuantThreads);
   const dim3 grid(static_cast<unsigned>(M));
   if (vpt <= 1)
-    quant_act_kernel<OutT, 1><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_kernel<OutT, 1, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   else if (vpt <= 2)
-    quant_act_kernel<OutT, 2><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_kernel<OutT, 2, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   else if (vpt <= 3)
-    quant_act_kernel<OutT, 3><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_kernel<OutT, 3, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   else if (vpt <= 4)
-    quant_act_kernel<OutT, 4><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_kernel<OutT, 4, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   else if (vpt <= 6)
-    quant_act_kernel<OutT, 6><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_kernel<OutT, 6, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   else if (vpt <= 8)
-    quant_act_kernel<OutT, 8><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_kernel<OutT, 8, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   else if (vpt <= 12)
-    quant_act_kernel<OutT, 12><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_kernel<OutT, 12, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   else if (vpt <= 16)
-    quant_act_kernel<OutT, 16><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_kernel<OutT, 16, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   else
-    quant_act_long_kernel<OutT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_long_kernel<OutT, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
   return cudaGetLastError();
 }
 
@@ -278,16 +313,59 @@ __global__ void __launch_bounds__(kQuantThreads) codes_s8_to_f16_kernel(const in
   if (threadIdx.x == 0) row_l1[m] = l1;
 }
 
+// Offset-binary INT4 (each nibble u holds the value u - 8: the "zp = 8" form
+// of the README's "Quantization" table) -> the library's two's complement
+// nibbles, (u - 8) mod 16 = u ^ 8 in each nibble.  16 bytes per thread and
+// step; the last n % 16 bytes one at a time.
+__global__ void __launch_bounds__(256) int4_from_offset_kernel(const uint8_t* src,
+                                                               uint8_t* dst,
+                                                               int64_t n) {
+  const int64_t n16 = n / 16;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n16; i += stride) {
+    uint4 v = reinterpret_cast<const uint4*>(src)[i];
+    v.x ^= 0x88888888u;
+    v.y ^= 0x88888888u;
+    v.z ^= 0x88888888u;
+    v.w ^= 0x88888888u;
+    reinterpret_cast<uint4*>(dst)[i] = v;
+  }
+  for (int64_t i = n16 * 16 + blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += stride)
+    dst[i] = static_cast<uint8_t>(src[i] ^ 0x88u);
+}
+
 }  // namespace
+
+cudaError_t launch_int4_from_offset(const uint8_t* src, uint8_t* dst, int64_t nbytes,
+                                    cudaStream_t st) {
+  const int64_t n16 = (nbytes + 15) / 16;
+  int64_t blocks = (n16 + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  int4_from_offset_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(src, dst, nbytes);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quant_act_s8(const __half* x, int64_t M, int64_t K, int8_t* q, float* sa,
                                 cudaStream_t st) {
-  return launch_quant_act<int8_t>(x, M, K, q, sa, nullptr, nullptr, 0, st);
+  return launch_quant_act<int8_t, __half>(x, M, K, q, sa, nullptr, nullptr, 0, st);
+}
+
+cudaError_t launch_quant_act_s8_bf16(const __nv_bfloat16* x, int64_t M, int64_t K, int8_t* q,
+                                     float* sa, cudaStream_t st) {
+  return launch_quant_act<int8_t, __nv_bfloat16>(x, M, K, q, sa, nullptr, nullptr, 0, st);
 }
 
 cudaError_t launch_quant_act_f16(const __half* x, int64_t M, int64_t K, __half* q, float* sa,
                                  int* row_l1, int* zero, int zero_words, cudaStream_t st) {
-  return launch_quant_act<__half>(x, M, K, q, sa, row_l1, zero, zero_words, st);
+  return launch_quant_act<__half, __half>(x, M, K, q, sa, row_l1, zero, zero_words, st);
+}
+
+cudaError_t launch_quant_act_f16_from_bf16(const __nv_bfloat16* x, int64_t M, int64_t K, __half* q,
+                                           float* sa, int* row_l1, int* zero, int zero_words,
+                                           cudaStream_t st) {
+  return launch_quant_act<__half, __nv_bfloat16>(x, M, K, q, sa, row_l1, zero, zero_words, st);
 }
 
 cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int group_size, bool int4,

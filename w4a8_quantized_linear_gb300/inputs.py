@@ -10,7 +10,8 @@ Recipe
   ``seed = base_seed + tensor_index`` in the fixed order x, W, x2, W2, ...
 * Activations x [M, K]: fp32 N(0, 1); ``floor(K / 100)`` outlier channels
   (1 % of K, sampled without replacement from the same generator) are scaled
-  by 20; the result is rounded to fp16.
+  by 20; the result is rounded to fp16 (or, for the bf16 entry points, to
+  bf16).
 * Weights W [N, K]: fp32 N(0, 0.02).
 """
 from __future__ import annotations
@@ -30,6 +31,20 @@ def activations(M: int, K: int, seed: int = 0) -> np.ndarray:
         cols = rng.choice(K, size=n_out, replace=False)
         x[:, cols] *= np.float32(OUTLIER_SCALE)
     return x.astype(np.float16)
+
+
+def activations_bf16(M: int, K: int, seed: int = 0) -> np.ndarray:
+    """The draws of :func:`activations`, rounded to bf16 (nearest, ties to
+    even) instead of fp16, as uint16 bit patterns [M, K] (numpy has no bf16
+    type; the upper half of each fp32, rounded)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x = rng.standard_normal((M, K), dtype=np.float32)
+    n_out = K // 100
+    if n_out:
+        cols = rng.choice(K, size=n_out, replace=False)
+        x[:, cols] *= np.float32(OUTLIER_SCALE)
+    b = x.view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
 
 
 def weights(N: int, K: int, seed: int = 1) -> np.ndarray:
