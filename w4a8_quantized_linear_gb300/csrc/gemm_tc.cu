@@ -263,13 +263,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         isum[j] = 0;
         fsum[j] = 0.0f;
       }
+      // per group: the weight scale of the next group is loaded while this
+      // group's accumulator is still being filled (a cache round trip after
+      // the wait would sit on every group's critical path)
+      const bool load_sw = PG && EPI == kEpiY && nvalid;
+      const float* swrow = p.sw + static_cast<int64_t>(n) * p.G;
+      float sw_next = load_sw ? __ldg(swrow) : 0.0f;
       for (int c = 0; c < nchunks; ++c, ++ch) {
         const int b = ch & 1;
+        const float swg = sw_next;
+        if (load_sw && c + 1 < nchunks) sw_next = __ldg(swrow + c + 1);
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(accf_bar(b), (ch >> 1) & 1, abort_flag,
                                                        err, kWaitTimeoutNs)))
           goto done;
         tc_fence_after();
-        const float swg = (PG && EPI == kEpiY && nvalid) ? __ldg(p.sw + static_cast<int64_t>(n) * p.G + c) : 0.0f;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t v[32];
@@ -293,20 +300,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(acce_bar(b));
       }
-      if (!nvalid || (PG && EPI == kEpiAcc)) continue;
-      const float swn = (!PG && EPI == kEpiY) ? __ldg(p.sw + n) : 0.0f;
+      if (PG && EPI == kEpiAcc) continue;
+      // the 64 token scales of this warp's columns: two per lane, handed out
+      // by shuffles (the whole warp takes part, also lanes past N)
+      float sa_lo = 0.0f, sa_hi = 0.0f;
+      if (EPI == kEpiY) {
+        if (m0 + lane < p.M) sa_lo = __ldg(p.sa + m0 + lane);
+        if (m0 + 32 + lane < p.M) sa_hi = __ldg(p.sa + m0 + 32 + lane);
+      }
+      const float swn = (!PG && EPI == kEpiY && nvalid) ? __ldg(p.sw + n) : 0.0f;
 #pragma unroll
       for (int j = 0; j < 64; ++j) {
         const int m = m0 + j;
-        if (m < p.M) {
+        const float sam = EPI == kEpiY ? __shfl_sync(0xffffffffu, j < 32 ? sa_lo : sa_hi, j & 31) : 0.0f;
+        if (nvalid && m < p.M) {
           const int64_t off = static_cast<int64_t>(m) * p.N + n;
           if (EPI == kEpiAcc) {
             p.acc[off] = isum[j];
           } else if (!PG) {
-            const float v = __fmul_rn(__fmul_rn(__int2float_rn(isum[j]), __ldg(p.sa + m)), swn);
+            const float v = __fmul_rn(__fmul_rn(__int2float_rn(isum[j]), sam), swn);
             p.y[off] = __float2half_rn(v);
           } else {
-            p.y[off] = __float2half_rn(__fmul_rn(fsum[j], __ldg(p.sa + m)));
+            p.y[off] = __float2half_rn(__fmul_rn(fsum[j], sam));
           }
         }
       }
