@@ -188,24 +188,28 @@ def kernel_source_sha(names=("gemm_pair.cu", "gemm_tc.cu", "gemv.cu", "cider_dev
     return h.hexdigest()[:16]
 
 
-def library_path(M: int, K: int, gs: int):
+def library_path(M: int, N: int, K: int, gs: int, bits: int = 8, num_sms: int = 152):
     """(dominant kernel, kernel launches per step) of the library's dispatch for
     one linear call: the same limits as gemv_fits() and launch_gemm_tc() in the
     CUDA sources (small-M GEMV up to M=16 when its activation block and a ring
-    of at least four 4 KiB weight tiles fit in shared memory, preceded by the
-    per-token quantization kernel unless M == 1 or M * K <= 8192; otherwise the
-    quantization kernel
-    followed by one tensor-core GEMM)."""
+    of at least four 4 KiB weight tiles fit in shared memory; it quantizes the
+    rows itself for one token or M * K <= 8192 unless it cuts K into slices,
+    which adds the quantization kernel and a combine kernel; otherwise the
+    quantization kernel followed by one tensor-core GEMM)."""
     if 1 <= M <= 16:
         mb = 1
         while mb < M:
             mb *= 2
         if mb * K <= 200 * 1024 and (227 * 1024 - 4096 - mb * K) // 4096 >= 4:
+            from w4a8_quantized_linear_gb300 import cider_debug_small_m_slices
+            slices = cider_debug_small_m_slices(M, N, K, bits, gs, num_sms)
+            form = "tensor-core form" if M >= 4 else "dp4a form"
+            if slices > 1:
+                return (f"gemv_kernel (small-M weight-streaming GEMV, {form}, K in {slices} "
+                        "slices + combine kernel)"), 3
             if M == 1 or M * K <= 8192:   # gemv_quantizes_itself()
                 return "gemv_kernel (small-M weight-streaming GEMV, fused quantization)", 1
-            if M >= 4:
-                return "gemv_kernel (small-M weight-streaming GEMV, tensor-core form)", 2
-            return "gemv_kernel (small-M weight-streaming GEMV on pre-quantized rows)", 2
+            return f"gemv_kernel (small-M weight-streaming GEMV, {form})", 2
     if gs:
         return "gemm_tc_kernel (tcgen05 kind::f16 on exact integer codes, per-group epilogue)", 2
     return "gemm_pair_kernel (tcgen05 cta_group::2 on CTA pairs, 256x256 tiles)", 2
@@ -444,7 +448,8 @@ def run_ours(a):
         return
 
     peaks, peak_src = measured_peaks()
-    kernel_name, launches_per_step = library_path(a.M, a.K, a.gs)
+    kernel_name, launches_per_step = library_path(
+        a.M, a.N, a.K, a.gs, a.bits, torch.cuda.get_device_properties(dev).multi_processor_count)
     small_m = kernel_name.startswith("gemv")
     wl = workload_name(a)
     if small_m:

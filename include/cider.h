@@ -244,6 +244,17 @@ cider_status_t cider_check_device_error(void* stream);
  * cider_check_device_error. */
 cider_status_t cider_debug_wait_timeout(int64_t max_polls, void* stream);
 
+/* K split of the small-M path (M <= 16), for inspection and the benchmark's
+ * launch count: pure host arithmetic, no GPU needed.  For a linear with y
+ * output on a GPU with num_sms SMs, writes the number of K slices the
+ * weight-streaming kernel uses (1: none; > 1: each row block's K is cut into
+ * that many slices on separate CTAs, the activation rows are quantized by a
+ * separate kernel first, and a second kernel adds the slices' partial sums and
+ * dequantizes).  int4 nonzero for W4A8.  Returns CIDER_ERR_INVALID_ARGUMENT
+ * for M outside [1, 16], N, K or num_sms < 1, or a NULL output. */
+cider_status_t cider_debug_small_m_slices(int64_t M, int64_t N, int64_t K, int int4,
+                                          int group_size, int num_sms, int32_t* slices);
+
 /* Work split of the per-channel tensor-core GEMM, for inspection and tests:
  * pure host arithmetic, no GPU needed.  For an M x N x K problem on `pairs`
  * CTA pairs (`pairs` >= 1 stands for the device's count), the GEMM's 256 x 256

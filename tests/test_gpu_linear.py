@@ -191,6 +191,30 @@ def test_whole_rounds_then_cut_tiles_all_outputs(cider, bits):
     assert_bits_equal(acc, oracle.gemm_acc(qa, qw_vals, 0), f"cut tiles acc bits={bits}")
 
 
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("gs", [0, 128])
+@pytest.mark.parametrize("M,N,K", [(2, 264, 8192), (5, 136, 6144), (16, 264, 8192),
+                                   (1, 520, 12288)])
+def test_small_m_split_k_all_outputs(cider, M, N, K, gs, bits):
+    """Few weight-row blocks with long rows: the small-M path cuts K into
+    slices on separate CTAs and adds their partial sums in a second kernel.
+    Every output against the oracle (per channel bit for bit), through both
+    the fused and the pre-quantized entry points."""
+    x = inputs.activations(M, K, seed=400 + M)
+    qw_dev, qw_vals, sw = make_weights(N, K, gs, bits, seed=401)
+    yref = oracle.linear(x, qw_vals, sw, gs, threads=8)
+    y = run_linear(cider, x, qw_dev, sw, gs, bits)
+    qa, sa = cider.cider_quantize_act(to_dev(x))
+    pre = cider.cider_w8a8_linear_prequant if bits == 8 else cider.cider_w4a8_linear_prequant
+    y2 = to_host(pre(qa, sa, to_dev(qw_dev), to_dev(sw), gs))
+    if gs == 0:
+        assert_bits_equal(y, yref, f"split-K small M={M} N={N} K={K} bits={bits}")
+        assert_bits_equal(y2, yref, f"split-K small prequant M={M} bits={bits}")
+    else:
+        assert_fp16_close(y, yref, f"split-K small M={M} N={N} K={K} gs={gs} bits={bits}")
+        assert_fp16_close(y2, yref, f"split-K small prequant M={M} gs={gs} bits={bits}")
+
+
 def test_no_device_error_left(cider):
     assert cider.cider_check_device_error() == 0
 

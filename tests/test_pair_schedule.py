@@ -135,3 +135,20 @@ def test_rejects_bad_arguments():
         cider_debug_pair_schedule(0, 256, 256, 76)
     with pytest.raises(CiderError):
         cider_debug_pair_schedule(256, 256, 256, 0)
+
+
+def test_small_m_path_cuts_k_only_for_long_rows_and_few_row_blocks():
+    from w4a8_quantized_linear_gb300 import CiderError, cider_debug_small_m_slices as slices
+    # many row blocks or short rows: one slice, as before
+    assert slices(1, 10240, 2560, 8, 0, 152) == 1
+    assert slices(16, 10240, 2560, 8, 0, 152) == 1
+    assert slices(16, 200, 2048, 8, 0, 152) == 1
+    # 160 row blocks of 40 (int8) or 20 (int4) weight tiles on 152 SMs: several slices
+    assert slices(16, 2560, 10240, 8, 0, 152) > 1
+    assert slices(16, 2560, 10240, 4, 128, 152) > 1
+    assert slices(1, 4096, 12288, 8, 128, 152) > 1
+    for M, N, K in [(1, 520, 12288), (2, 264, 8192), (5, 136, 6144), (16, 264, 8192)]:
+        ks = slices(M, N, K, 8, 0, 152)
+        assert 2 <= ks <= 16
+    with pytest.raises(CiderError):
+        slices(17, 256, 256, 8, 0, 152)

@@ -63,6 +63,7 @@ def _declare(lib):
         "cider_timing_end": ([ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)], i32),
         "cider_debug_wait_timeout": ([i64, p], i32),
         "cider_debug_pair_schedule": ([i64, i64, i64, i32, i64, p, p, p], i32),
+        "cider_debug_small_m_slices": ([i64, i64, i64, i32, i32, i32, p], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -304,3 +305,13 @@ def cider_debug_pair_schedule(M: int, N: int, K: int, pairs: int):
     keys = ("pairs", "whole_tiles", "cut_tiles", "pieces", "blocks_per_tile", "tiles")
     units = [tuple(rows[7 * i:7 * i + 7]) for i in range(count.value)]
     return dict(zip(keys, list(info))), units
+
+
+def cider_debug_small_m_slices(M: int, N: int, K: int, bits: int, group_size: int,
+                               num_sms: int) -> int:
+    """K slices of the small-M path for this linear (host arithmetic only)."""
+    out = ctypes.c_int32(0)
+    _check("cider_debug_small_m_slices",
+           _load().cider_debug_small_m_slices(M, N, K, 1 if bits == 4 else 0, group_size,
+                                              num_sms, ctypes.byref(out)))
+    return int(out.value)

@@ -224,27 +224,37 @@ cider_status_t run_linear(const LinearArgs& a) {
     // small M: for one token or short rows the GEMV quantizes the rows itself
     // (every CTA repeats that work, cheaper than a second launch for so few
     // values); otherwise one quantization kernel writes the int8 codes first.
-    // bf16 rows always go through the quantization kernel (the GEMV stages fp16).
+    // bf16 rows, and problems whose K is split over several CTAs per row
+    // block, always take the quantization kernel.
+    const size_t pbytes = cider::gemv_part_bytes(a.M, a.N, a.K, a.int4, gs, a.mode, sms);
     const __half* xg = static_cast<const __half*>(a.x);
     const int8_t* qa = a.qa;
     const float* sa = a.sa;
-    if (a.x && (a.x_bf16 || !cider::gemv_quantizes_itself(a.M, a.K))) {
-      const size_t qbytes = round_up(static_cast<size_t>(a.M * a.K), 256);
-      cudaError_t e = scratch_alloc(scratch, dev, qbytes + round_up(4 * a.M, 256), a.st);
+    void* part = nullptr;
+    const bool quantize_first =
+        a.x && (a.x_bf16 || pbytes > 0 || !cider::gemv_quantizes_itself(a.M, a.K));
+    const size_t qbytes = quantize_first ? round_up(static_cast<size_t>(a.M * a.K), 256) : 0;
+    const size_t sbytes = quantize_first ? round_up(4 * a.M, 256) : 0;
+    if (qbytes + sbytes + pbytes > 0) {
+      cudaError_t e = scratch_alloc(scratch, dev, qbytes + sbytes + round_up(pbytes, 256), a.st);
       if (e != cudaSuccess) return cuda_status(e);
-      int8_t* qs = static_cast<int8_t*>(scratch.ptr);
-      float* ss = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch.ptr) + qbytes);
-      e = a.x_bf16 ? cider::launch_quant_act_s8_bf16(static_cast<const __nv_bfloat16*>(a.x), a.M,
-                                                     a.K, qs, ss, a.st)
-                   : cider::launch_quant_act_s8(xg, a.M, a.K, qs, ss, a.st);
-      if (e != cudaSuccess) return cuda_status(e);
-      xg = nullptr;
-      qa = qs;
-      sa = ss;
+      uint8_t* base = static_cast<uint8_t*>(scratch.ptr);
+      if (pbytes > 0) part = base + qbytes + sbytes;
+      if (quantize_first) {
+        int8_t* qs = reinterpret_cast<int8_t*>(base);
+        float* ss = reinterpret_cast<float*>(base + qbytes);
+        e = a.x_bf16 ? cider::launch_quant_act_s8_bf16(static_cast<const __nv_bfloat16*>(a.x), a.M,
+                                                       a.K, qs, ss, a.st)
+                     : cider::launch_quant_act_s8(xg, a.M, a.K, qs, ss, a.st);
+        if (e != cudaSuccess) return cuda_status(e);
+        xg = nullptr;
+        qa = qs;
+        sa = ss;
+      }
     }
     return cuda_status(timed_launch(a.st, [&] {
       return cider::launch_gemv(xg, qa, sa, a.M, a.N, a.K, w, a.int4, a.sw, gs, a.mode, y, a.acc,
-                                sms, a.st);
+                                part, sms, a.st);
     }));
   }
   // tensor-core path: activation codes as fp16 integers, scales, row sums of |code|
@@ -531,6 +541,16 @@ cider_status_t cider_debug_wait_timeout(int64_t max_polls, void* stream) {
     cider_status_t s = check_device(nullptr, nullptr);
     if (s != CIDER_OK) return s;
     return cuda_status(cider::launch_debug_wait_timeout(max_polls, static_cast<cudaStream_t>(stream)));
+  });
+}
+
+cider_status_t cider_debug_small_m_slices(int64_t M, int64_t N, int64_t K, int int4,
+                                          int group_size, int num_sms, int32_t* slices) {
+  return guarded([&] {
+    if (M < 1 || M > 16 || N < 1 || K < 1 || num_sms < 1 || slices == nullptr)
+      return CIDER_ERR_INVALID_ARGUMENT;
+    *slices = cider::gemv_slices(M, N, K, int4 != 0, group_size, cider::kEpiY, num_sms);
+    return CIDER_OK;
   });
 }
 

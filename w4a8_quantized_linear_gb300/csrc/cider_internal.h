@@ -70,9 +70,17 @@ bool gemv_fits(int64_t M, int64_t K);
 // itself (every CTA repeats that work) rather than run a quantization kernel
 // first: for one token, or while the rows are short (measured on GB300).
 inline bool gemv_quantizes_itself(int64_t M, int64_t K) { return M == 1 || M * K <= 8192; }
+// K split of the small-M path (few weight-row blocks, long rows): the bytes of
+// partial sums it needs for this problem (0: no split); the split needs
+// pre-quantized rows (qa, sa) and y output.
+size_t gemv_part_bytes(int64_t M, int64_t N, int64_t K, bool int4, int group_size, int mode,
+                       int num_sms);
+// The number of K slices it uses (1: none).  Host arithmetic only.
+int gemv_slices(int64_t M, int64_t N, int64_t K, bool int4, int group_size, int mode,
+                int num_sms);
 cudaError_t launch_gemv(const __half* x, const int8_t* qa, const float* sa, int64_t M, int64_t N,
                         int64_t K, const uint8_t* w, bool int4, const float* sw, int group_size,
-                        int mode, __half* y, int32_t* acc, int num_sms, cudaStream_t st);
+                        int mode, __half* y, int32_t* acc, void* part, int num_sms, cudaStream_t st);
 
 // gemm_tc.cu: tensor-core path.  qa16 holds the activation codes as fp16
 // integers [M, K]; row_l1[m] = sum_k |code| (used by the per-channel kernel

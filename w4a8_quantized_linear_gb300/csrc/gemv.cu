@@ -84,15 +84,21 @@ struct GemvArgs {
   int64_t N;
   const float* sw;
   int gs, G, NS;
+  int ks, tps, Ka;    // K slices, tiles per slice, staged codes per token row
   __half* y;
   int32_t* acc;
+  uint32_t* part;     // ks > 1: partial sums [ks][M][N] (int32 per channel, fp32 per group)
   int* err;
 };
 
 // The weight matrix streams through a ring of NS tiles of 16 rows x 256
 // bytes, loaded by TMA (one 2D box per tile, zero-filled past N and past the
 // end of a row) by the producer warp.  CTA c takes row blocks c, c + grid, ...
-// and for each the tiles along K.  Consumer warp w owns rows 2w, 2w+1 of the
+// and for each the tiles along K.  With K split into ks slices (few row
+// blocks, long rows), CTA c takes slice c % ks of row blocks c / ks,
+// c / ks + grid / ks, ..., stages only that slice's activation codes, and
+// writes partial sums that gemv_combine_kernel adds up and dequantizes.
+// Consumer warp w owns rows 2w, 2w+1 of the
 // block; lane l works on row 2w + l/16 and on its 16-byte chunk l%16 of each
 // tile, accumulating over the tiles of the block, and the 16 lanes of a row
 // are reduced at the block's end.
@@ -119,6 +125,15 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   const int ntk = static_cast<int>((rowbytes + kBoxBytes - 1) / kBoxBytes);  // tiles per block
   const int64_t nblocks = (N + kBoxRows - 1) / kBoxRows;
   const int nchunks = K / VALS;
+  // this CTA's K slice (the whole row when ks == 1)
+  constexpr int kCodesPerTile = INT4 ? 2 * kBoxBytes : kBoxBytes;
+  const int ks = p.ks;
+  const int slice = static_cast<int>(blockIdx.x) % ks;
+  const int64_t b_first = blockIdx.x / ks, b_step = gridDim.x / ks;
+  const int kt0 = slice * p.tps;
+  const int kt1 = kt0 + p.tps < ntk ? kt0 + p.tps : ntk;
+  const int kbase = kt0 * kCodesPerTile;   // first code of the slice
+  const int Ka = p.Ka;                     // row stride of the staged codes
 
   if (threadIdx.x == 0) {
     s_abort = 0u;
@@ -135,8 +150,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     if (lane == 0) {
       prefetch_tensormap(&tmW);
       int it = 0;
-      for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x)
-        for (int kt = 0; kt < ntk; ++kt, ++it) {
+      for (int64_t b = b_first; b < nblocks; b += b_step)
+        for (int kt = kt0; kt < kt1; ++kt, ++it) {
           const int s = it % NS;
           if (!mbar_wait_bounded(smem_u32(&s_empty[s]), ((it / NS) & 1) ^ 1u, &s_abort, p.err,
                                  kKernelWaitTimeoutNs))
@@ -221,13 +236,15 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       }
     }
   } else {
-    const int n16 = K / 16;
+    // codes [kbase, kbase + Ka) of every token row (zeros past K and past M)
+    const int n16 = Ka / 16;
     for (int i = ctid; i < MB * n16; i += cthreads) {
       const int m = i / n16, c = i - m * n16;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (m < M) v = *reinterpret_cast<const uint4*>(p.qa + static_cast<int64_t>(m) * K + c * 16);
+      if (m < M && kbase + c * 16 < K)
+        v = *reinterpret_cast<const uint4*>(p.qa + static_cast<int64_t>(m) * K + kbase + c * 16);
       const uint2 a = arrange8<INT4>(v.x, v.y), b = arrange8<INT4>(v.z, v.w);
-      *reinterpret_cast<uint4*>(s_act + static_cast<size_t>(m) * K + c * 16) = make_uint4(a.x, a.y, b.x, b.y);
+      *reinterpret_cast<uint4*>(s_act + static_cast<size_t>(m) * Ka + c * 16) = make_uint4(a.x, a.y, b.x, b.y);
     }
     if (ctid < MB) s_sa[ctid] = (p.sa != nullptr && ctid < M) ? p.sa[ctid] : 0.0f;
   }
@@ -241,10 +258,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     const int g8 = lane >> 2, t4 = lane & 3;
     // fragment k order: in k-step j, thread t4 holds codes 16 t4 + 4 j .. + 3
     // of its quarter for both operands (the same permutation of K for A and B)
-    const uint8_t* arow0 = s_act + static_cast<size_t>(g8) * K;
-    const uint8_t* arow1 = s_act + static_cast<size_t>(g8 + 8) * K;
+    // staged rows start at code kbase: the code at k lives at row + (k - kbase)
+    const uint8_t* arow0 = s_act + static_cast<size_t>(g8) * Ka;
+    const uint8_t* arow1 = s_act + static_cast<size_t>(g8 + 8) * Ka;
     int it = 0;
-    for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
+    for (int64_t b = b_first; b < nblocks; b += b_step) {
       int iacc[8];    // [n-block][4]: tokens g8 (0, 1) / g8 + 8 (2, 3), rows 2 t4 (+1)
       float facc[8];
 #pragma unroll
@@ -252,7 +270,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         iacc[i] = 0;
         facc[i] = 0.0f;
       }
-      for (int kt = 0; kt < ntk; ++kt, ++it) {
+      for (int kt = kt0; kt < kt1; ++kt, ++it) {
         if ((it & 1) != par) continue;
         const int s = it % NS;
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&s_full[s]), (it / NS) & 1,
@@ -283,8 +301,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
           // thread t4 holds codes 16 t4 .. + 15 of the quarter; k-step j uses its word j
           const int k0 = kt * kBoxBytes + q * 64 + 16 * t4;
           uint4 al = make_uint4(0u, 0u, 0u, 0u), ah = al;
-          if (k0 < K && g8 < MB) al = *reinterpret_cast<const uint4*>(arow0 + k0);
-          if (k0 < K && MB == 16) ah = *reinterpret_cast<const uint4*>(arow1 + k0);
+          if (k0 < K && g8 < MB) al = *reinterpret_cast<const uint4*>(arow0 + (k0 - kbase));
+          if (k0 < K && MB == 16) ah = *reinterpret_cast<const uint4*>(arow1 + (k0 - kbase));
           const uint4 w0 = *reinterpret_cast<const uint4*>(wt + g8 * kBoxBytes + 16 * t4);
           const uint4 w1 = *reinterpret_cast<const uint4*>(wt + (8 + g8) * kBoxBytes + 16 * t4);
           __syncwarp();
@@ -313,8 +331,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
           for (int h = 0; h < 2; ++h) {
             const int k0 = cb + 64 * h + 16 * t4;
             uint4 al = make_uint4(0u, 0u, 0u, 0u), ah = al;
-            if (k0 < K && g8 < MB) al = *reinterpret_cast<const uint4*>(arow0 + k0);
-            if (k0 < K && MB == 16) ah = *reinterpret_cast<const uint4*>(arow1 + k0);
+            if (k0 < K && g8 < MB) al = *reinterpret_cast<const uint4*>(arow0 + (k0 - kbase));
+            if (k0 < K && MB == 16) ah = *reinterpret_cast<const uint4*>(arow1 + (k0 - kbase));
             const uint2 w0 = *reinterpret_cast<const uint2*>(wt + g8 * kBoxBytes + 32 * h + 8 * t4);
             const uint2 w1 = *reinterpret_cast<const uint2*>(wt + (8 + g8) * kBoxBytes + 32 * h + 8 * t4);
             if (h == 1) {
@@ -362,13 +380,18 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             for (int w = 0; w < kGemvWarps; ++w) v += s_red[w][src];
             if (EPI == kEpiAcc)
               p.acc[off] = v;
+            else if (ks > 1)
+              p.part[(static_cast<int64_t>(slice) * M + m) * N + n] = static_cast<uint32_t>(v);
             else
               p.y[off] = __float2half_rn(__fmul_rn(__fmul_rn(__int2float_rn(v), s_sa[m]), __ldg(p.sw + n)));
           } else {
             float v = 0.0f;
 #pragma unroll
             for (int w = 0; w < kGemvWarps; ++w) v += __int_as_float(s_red[w][src]);
-            p.y[off] = __float2half_rn(v);
+            if (ks > 1)
+              p.part[(static_cast<int64_t>(slice) * M + m) * N + n] = __float_as_uint(v);
+            else
+              p.y[off] = __float2half_rn(v);
           }
         }
       }
@@ -379,7 +402,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   const int rl = 2 * warp + (lane >> 4);  // row within the block
   const int ch = lane & 15;               // 16-byte chunk within the tile row
   int it = 0;
-  for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
+  for (int64_t b = b_first; b < nblocks; b += b_step) {
     const int64_t n = b * kBoxRows + rl;
     const bool nvalid = n < N;
     int acc[MB];
@@ -389,7 +412,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       acc[m] = 0;
       fs[m] = 0.0f;
     }
-    for (int kt = 0; kt < ntk; ++kt, ++it) {
+    for (int kt = kt0; kt < kt1; ++kt, ++it) {
       const int s = it % NS;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&s_full[s]), (it / NS) & 1, &s_abort,
                                                      p.err, kKernelWaitTimeoutNs)))
@@ -419,7 +442,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       for (int m = 0; m < MB; ++m) {
         uint4 a0 = make_uint4(0u, 0u, 0u, 0u), a1 = a0;
         if (live) {
-          const uint8_t* ap = s_act + static_cast<size_t>(m) * K + static_cast<size_t>(c) * VALS;
+          // staged rows start at code kbase
+          const uint8_t* ap = s_act + static_cast<size_t>(m) * Ka + (c * VALS - kbase);
           a0 = *reinterpret_cast<const uint4*>(ap);
           if (INT4) a1 = *reinterpret_cast<const uint4*>(ap + 16);
         }
@@ -468,6 +492,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         const int64_t off = static_cast<int64_t>(m) * N + n;
         if (EPI == kEpiAcc) {
           p.acc[off] = static_cast<int32_t>(bits);
+        } else if (ks > 1) {
+          p.part[(static_cast<int64_t>(slice) * M + m) * N + n] = bits;
         } else if (!PG) {
           p.y[off] = __float2half_rn(
               __fmul_rn(__fmul_rn(__int2float_rn(static_cast<int>(bits)), s_sa[m]), __ldg(p.sw + n)));
@@ -487,14 +513,91 @@ int ring_slots(int64_t MB, int64_t K, bool mma = false) {
   return static_cast<int>(ns);
 }
 
+// Partial sums of the K slices -> y: per channel the exact int32 sum, then
+// (acc * s_a) * s_w; per group the fp32 sum of the slices' partials, times
+// s_a unless the partials already carry it (tensor-core form).
+template <bool PG, bool PG_SCALED>
+__global__ void __launch_bounds__(256) gemv_combine_kernel(const uint32_t* __restrict__ part,
+                                                           int ks, int M, int64_t N,
+                                                           const float* __restrict__ sa,
+                                                           const float* __restrict__ sw,
+                                                           __half* __restrict__ y) {
+  const int64_t total = static_cast<int64_t>(M) * N;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int m = static_cast<int>(i / N);
+    const int64_t n = i - static_cast<int64_t>(m) * N;
+    if (!PG) {
+      int v = 0;
+      for (int s = 0; s < ks; ++s) v += static_cast<int>(part[s * total + i]);
+      y[i] = __float2half_rn(__fmul_rn(__fmul_rn(__int2float_rn(v), __ldg(sa + m)), __ldg(sw + n)));
+    } else {
+      float v = 0.0f;
+      for (int s = 0; s < ks; ++s) v += __uint_as_float(part[s * total + i]);
+      y[i] = __float2half_rn(PG_SCALED ? v : __fmul_rn(v, __ldg(sa + m)));
+    }
+  }
+}
+
+// K split of the small-M path: ks slices of tps weight tiles, Ka codes staged
+// per token row.
+struct GemvSplit {
+  int ks, tps, Ka;
+};
+
+// Cost model (in weight tiles streamed by one CTA): rounds of (row block,
+// slice) units over the resident CTAs times tiles per unit, plus ~2 tiles for
+// the combine launch.  Resident CTAs per SM are estimated from shared memory
+// and, for registers, as 2 for the tensor-core form and 4 for the dp4a form
+// (the kernels' measured register counts).  A split must win by 20 %.
+GemvSplit gemv_plan(int64_t MB, int64_t N, int64_t K, bool int4, bool mma, bool allow,
+                    int num_sms) {
+  const int64_t rowbytes = int4 ? K / 2 : K;
+  const int ntk = static_cast<int>((rowbytes + kBoxBytes - 1) / kBoxBytes);
+  const int cpt = int4 ? 2 * kBoxBytes : kBoxBytes;
+  const int64_t nblocks = (N + kBoxRows - 1) / kBoxRows;
+  GemvSplit best{1, ntk, static_cast<int>(K)};
+  auto cost = [&](int tps, int kse, int Ka) {
+    int ns = ring_slots(MB, Ka, mma);
+    if (ns > 8) ns = 8;
+    const int64_t sm = static_cast<int64_t>(ns) * kTileBytes + MB * Ka + 1024;
+    int64_t occ = (228 * 1024) / (sm + (mma ? kRedBytes : 0) + 2 * 1024);
+    const int64_t cap = mma ? 2 : 4;
+    if (occ > cap) occ = cap;
+    if (occ < 1) occ = 1;
+    const int64_t slots = static_cast<int64_t>(num_sms) * occ;
+    const int64_t units = nblocks * kse;
+    return static_cast<double>((units + slots - 1) / slots) * tps + (kse > 1 ? 2.0 : 0.0);
+  };
+  // only long rows: with few tiles per row block one CTA's chain is short
+  // and the extra launches (quantization, combine) cost more than they save
+  if (!allow || ntk < 16) return best;
+  const double c1 = cost(ntk, 1, static_cast<int>(K));
+  double bc = c1;
+  for (int ks = 2; ks <= 16 && ntk / ks >= 2; ++ks) {
+    const int tps = (ntk + ks - 1) / ks;
+    const int kse = (ntk + tps - 1) / tps;
+    if (kse != ks) continue;
+    const int64_t ka = static_cast<int64_t>(tps) * cpt;
+    const int Ka = static_cast<int>(ka < K ? ka : K);
+    const double c = cost(tps, kse, Ka);
+    if (c < bc && c < 0.8 * c1) {
+      bc = c;
+      best = GemvSplit{kse, tps, Ka};
+    }
+  }
+  return best;
+}
+
 template <int MB, bool INT4, bool PG, int EPI, bool FUSEQ, bool MMA>
 cudaError_t launch_one(const __half* x, const int8_t* qa, const float* sa, int64_t M, int64_t N,
                        int64_t K, const uint8_t* w, const float* sw, int gs, __half* y,
-                       int32_t* acc, int num_sms, cudaStream_t st) {
+                       int32_t* acc, const GemvSplit& sp, uint32_t* part, int num_sms,
+                       cudaStream_t st) {
   auto kern = gemv_kernel<MB, INT4, PG, EPI, FUSEQ, MMA>;
-  const int NS = ring_slots(MB, K, MMA);
+  const int NS = ring_slots(MB, sp.Ka, MMA);
   if (NS < 4) return cudaErrorInvalidValue;
-  const size_t smem = static_cast<size_t>(NS) * kTileBytes + static_cast<size_t>(MB) * K + 1024;
+  const size_t smem = static_cast<size_t>(NS) * kTileBytes + static_cast<size_t>(MB) * sp.Ka + 1024;
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern),
                                           kSmemBudget - (MMA ? kRedBytes : 0) + 1024, attr_done);
@@ -515,8 +618,12 @@ cudaError_t launch_one(const __half* x, const int8_t* qa, const float* sa, int64
   a.gs = gs;
   a.G = gs > 0 ? static_cast<int>(K / gs) : 1;
   a.NS = NS;
+  a.ks = sp.ks;
+  a.tps = sp.tps;
+  a.Ka = sp.Ka;
   a.y = y;
   a.acc = acc;
+  a.part = part;
   e = device_error_word(&a.err);
   if (e != cudaSuccess) return e;
   // Resident CTAs per SM from shared memory and the kernel's registers
@@ -536,26 +643,40 @@ cudaError_t launch_one(const __half* x, const int8_t* qa, const float* sa, int64
   if (occ > 2048 / kGemvThreads) occ = 2048 / kGemvThreads;
   if (occ < 1) occ = 1;
   const int64_t nblocks = (N + kBoxRows - 1) / kBoxRows;
-  int64_t blocks = nblocks;
+  int64_t blocks = nblocks * sp.ks;   // (row block, slice) units
   const int64_t cap = static_cast<int64_t>(num_sms) * occ;
-  if (blocks > cap) blocks = cap;
+  if (blocks > cap) blocks = cap / sp.ks * sp.ks;   // every CTA keeps one slice
   kern<<<static_cast<unsigned>(blocks), kGemvThreads, smem, st>>>(tmW, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || sp.ks == 1) return e;
+  const int64_t total = M * N;
+  const unsigned cb = static_cast<unsigned>((total + 255) / 256 < 1024 ? (total + 255) / 256 : 1024);
+  gemv_combine_kernel<PG, PG && MMA><<<cb, 256, 0, st>>>(part, sp.ks, static_cast<int>(M), N, sa,
+                                                         sw, y);
   return cudaGetLastError();
+}
+
+// The tensor-core form serves 4..16 tokens, int8 or int4 weights (not the
+// exact per-group accumulators, which keep the dp4a lanes' group reductions).
+bool gemv_uses_mma(int64_t MB, int64_t K, bool pg, int mode) {
+  return MB >= 4 && !(pg && mode == kEpiAcc) && ring_slots(MB, K, true) >= 4;
 }
 
 template <int MB>
 cudaError_t dispatch_mb(const __half* x, const int8_t* qa, const float* sa, int64_t M, int64_t N,
                         int64_t K, const uint8_t* w, bool int4, const float* sw, int gs, int mode,
-                        __half* y, int32_t* acc, int num_sms, cudaStream_t st) {
+                        __half* y, int32_t* acc, uint32_t* part, int num_sms, cudaStream_t st) {
   const bool pg = gs > 0;
   const bool fq = x != nullptr;
-  // tensor-core form for 4..16 tokens, int8 or int4 weights (not for the
-  // exact per-group accumulators, which keep the dp4a lanes' group reductions)
   constexpr bool kMmaMB = MB >= 4;
-  if (kMmaMB && !(pg && mode == kEpiAcc) && ring_slots(MB, K, true) >= 4) {
+  const bool mma = gemv_uses_mma(MB, K, pg, mode);
+  const GemvSplit sp = gemv_plan(MB, N, K, int4, mma, part != nullptr && !fq && mode == kEpiY,
+                                 num_sms);
+  if (kMmaMB && mma) {
 #define CIDER_GEMV_MMA_CASE(I4, P, E, F)                                                      \
   if (int4 == I4 && pg == P && mode == E && fq == F)                                          \
-    return launch_one<MB, I4, P, E, F, kMmaMB>(x, qa, sa, M, N, K, w, sw, gs, y, acc, num_sms, st);
+    return launch_one<MB, I4, P, E, F, kMmaMB>(x, qa, sa, M, N, K, w, sw, gs, y, acc, sp, part,    \
+                                               num_sms, st);
     CIDER_GEMV_MMA_CASE(false, false, kEpiY, true)
     CIDER_GEMV_MMA_CASE(false, true, kEpiY, true)
     CIDER_GEMV_MMA_CASE(false, false, kEpiY, false)
@@ -570,7 +691,8 @@ cudaError_t dispatch_mb(const __half* x, const int8_t* qa, const float* sa, int6
   }
 #define CIDER_GEMV_CASE(I4, P, E, F)                                                          \
   if (int4 == I4 && pg == P && mode == E && fq == F)                                          \
-    return launch_one<MB, I4, P, E, F, false>(x, qa, sa, M, N, K, w, sw, gs, y, acc, num_sms, st);
+    return launch_one<MB, I4, P, E, F, false>(x, qa, sa, M, N, K, w, sw, gs, y, acc, sp, part,     \
+                                              num_sms, st);
   CIDER_GEMV_CASE(false, false, kEpiY, true)
   CIDER_GEMV_CASE(false, true, kEpiY, true)
   CIDER_GEMV_CASE(true, false, kEpiY, true)
@@ -596,14 +718,29 @@ bool gemv_fits(int64_t M, int64_t K) {
   return mb * K <= kSmemActMax && ring_slots(mb, K) >= 4;
 }
 
+int gemv_slices(int64_t M, int64_t N, int64_t K, bool int4, int group_size, int mode,
+                int num_sms) {
+  if (mode != kEpiY) return 1;
+  int64_t mb = 1;
+  while (mb < M) mb *= 2;
+  return gemv_plan(mb, N, K, int4, gemv_uses_mma(mb, K, group_size > 0, mode), true, num_sms).ks;
+}
+
+size_t gemv_part_bytes(int64_t M, int64_t N, int64_t K, bool int4, int group_size, int mode,
+                       int num_sms) {
+  const int ks = gemv_slices(M, N, K, int4, group_size, mode, num_sms);
+  return ks > 1 ? static_cast<size_t>(ks) * M * N * 4 : 0;
+}
+
 cudaError_t launch_gemv(const __half* x, const int8_t* qa, const float* sa, int64_t M, int64_t N,
                         int64_t K, const uint8_t* w, bool int4, const float* sw, int group_size,
-                        int mode, __half* y, int32_t* acc, int num_sms, cudaStream_t st) {
-  if (M <= 1) return dispatch_mb<1>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, num_sms, st);
-  if (M <= 2) return dispatch_mb<2>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, num_sms, st);
-  if (M <= 4) return dispatch_mb<4>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, num_sms, st);
-  if (M <= 8) return dispatch_mb<8>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, num_sms, st);
-  return dispatch_mb<16>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, num_sms, st);
+                        int mode, __half* y, int32_t* acc, void* part, int num_sms, cudaStream_t st) {
+  uint32_t* pp = static_cast<uint32_t*>(part);
+  if (M <= 1) return dispatch_mb<1>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, pp, num_sms, st);
+  if (M <= 2) return dispatch_mb<2>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, pp, num_sms, st);
+  if (M <= 4) return dispatch_mb<4>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, pp, num_sms, st);
+  if (M <= 8) return dispatch_mb<8>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, pp, num_sms, st);
+  return dispatch_mb<16>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, pp, num_sms, st);
 }
 
 }  // namespace cider

@@ -118,7 +118,7 @@ extern "C" cider_status_t cider_w8a8_linear_noalloc(const void* x, int64_t M, in
     (void)base;
     if (cider::gemv_fits(M, K)) {
       e = cider::launch_gemv(static_cast<const __half*>(x), nullptr, nullptr, M, N, K, w, false, sw,
-                             group_size, cider::kEpiY, yh, nullptr, sms, st);
+                             group_size, cider::kEpiY, yh, nullptr, /*no K split*/ nullptr, sms, st);
     } else {
       const size_t qbytes = round256(2 * static_cast<size_t>(M) * static_cast<size_t>(K));
       const size_t vbytes = round256(4 * static_cast<size_t>(M));
