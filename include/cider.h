@@ -194,7 +194,7 @@ cider_status_t cider_w4a8_accumulators(const int8_t* qa, int64_t M, int64_t N,
  * of device global memory per GPU on which the library has been used. */
 #define CIDER_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
-/* W8A8 linear that allocates no memory.  The paper has no counterpart: this
+/* W8A8 linear that allocates no memory.  The Cider README has no counterpart: this
  * entry exists for callers that must not allocate device memory while they
  * run, for example an inference engine that reserved almost all of HBM for
  * weights and KV cache before serving, or a decode loop that cannot let a
