@@ -134,3 +134,36 @@ def test_binding_fails_loudly_without_library(monkeypatch):
 def test_timing_argument_checks(lib):
     assert lib.cider_timing_begin(0) == INVALID
     assert lib.cider_timing_end(None, None) == INVALID
+
+
+@pytest.mark.parametrize("fn", ["cider_w8a8_linear_bf16", "cider_w4a8_linear_bf16"])
+def test_bf16_linears_check_like_the_fp16_ones(lib, no_device, fn):
+    assert lin(lib, fn=fn) == UNSUPPORTED
+    assert lin(lib, fn=fn, x=None) == INVALID
+    assert lin(lib, fn=fn, N=12) == INVALID
+    assert lin(lib, fn=fn, gran=1, gs=32) == INVALID
+    assert lin(lib, fn=fn, x=P + 8) == MISALIGNED
+    assert lin(lib, fn=fn, M=0, x=None, w=None, sw=None, y=None) == OK
+
+
+def test_bf16_quantize_and_int4_import_argument_checks(lib, no_device):
+    assert lib.cider_quantize_act_bf16(P, 4, 256, P, P, None) == UNSUPPORTED
+    assert lib.cider_quantize_act_bf16(P, 4, 100, P, P, None) == INVALID
+    assert lib.cider_quantize_act_bf16(P + 8, 4, 256, P, P, None) == MISALIGNED
+    assert lib.cider_quantize_act_bf16(None, 0, 256, None, None, None) == OK
+    assert lib.cider_int4_from_offset_binary(P, P, 1000, None) == UNSUPPORTED
+    assert lib.cider_int4_from_offset_binary(P, P, 0, None) == OK
+    assert lib.cider_int4_from_offset_binary(P, P, -1, None) == INVALID
+    assert lib.cider_int4_from_offset_binary(None, P, 16, None) == INVALID
+    assert lib.cider_int4_from_offset_binary(P + 4, P, 16, None) == MISALIGNED
+
+
+def test_debug_split_queries_need_no_device(lib):
+    n = ctypes.c_int64(0)
+    info = (ctypes.c_int32 * 6)()
+    assert lib.cider_debug_pair_schedule(4096, 10240, 2560, 76, 0, None, ctypes.byref(n), info) == OK
+    assert n.value > 0 and info[0] == 76
+    ks = ctypes.c_int32(0)
+    assert lib.cider_debug_small_m_slices(16, 2560, 10240, 0, 0, 152, ctypes.byref(ks)) == OK
+    assert ks.value > 1
+    assert lib.cider_debug_small_m_slices(0, 2560, 10240, 0, 0, 152, ctypes.byref(ks)) == INVALID
