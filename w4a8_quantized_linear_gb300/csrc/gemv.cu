@@ -97,11 +97,11 @@ struct GemvArgs {
 // and for each the tiles along K.  With K split into ks slices (few row
 // blocks, long rows), CTA c takes slice c % ks of row blocks c / ks,
 // c / ks + grid / ks, ..., stages only that slice's activation codes, and
-// writes partial sums that gemv_combine_kernel adds up and dequantizes.
-// Consumer warp w owns rows 2w, 2w+1 of the
-// block; lane l works on row 2w + l/16 and on its 16-byte chunk l%16 of each
-// tile, accumulating over the tiles of the block, and the 16 lanes of a row
-// are reduced at the block's end.
+// writes partial sums that gemv_combine_kernel adds up and dequantizes.  In
+// the dp4a form consumer warp w owns rows 2w, 2w+1 of the block; lane l works
+// on row 2w + l/16 and on its 16-byte chunk l%16 of each tile, accumulating
+// over the tiles of the block, and the 16 lanes of a row are reduced at the
+// block's end.
 template <int MB, bool INT4, bool PG, int EPI, bool FUSEQ, bool MMA>
 __global__ void __launch_bounds__(kGemvThreads, 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tmW, const GemvArgs p) {
