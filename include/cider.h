@@ -199,13 +199,18 @@ cider_status_t cider_w4a8_accumulators(const int8_t* qa, int64_t M, int64_t N,
  * run, for example an inference engine that reserved almost all of HBM for
  * weights and KV cache before serving, or a decode loop that cannot let a
  * memory pool grow (growth can fail under memory pressure or wait on the
- * driver).  Arguments, results and checks are those of cider_w8a8_linear;
- * the scratch it needs (none for M <= 16; else activation codes, per-token
- * scales and per-token code sums, 2*M*K + 4*M + 4*M bytes, each part
- * rounded up to 256-byte blocks) comes from one fixed array of
- * CIDER_NOALLOC_SCRATCH_BYTES in device memory instead of a pool; a problem
- * that needs more returns CIDER_ERR_INVALID_ARGUMENT (for K = 2560: M above
- * 6543).
+ * driver).  Arguments, results, checks and kernels are those of
+ * cider_w8a8_linear; its scratch comes from one fixed array of
+ * CIDER_NOALLOC_SCRATCH_BYTES in device memory instead of a pool.  Required
+ * scratch, each part rounded up to 256-byte blocks: none for M <= 16 when
+ * M == 1 or M * K <= 8192 (the small-M kernel quantizes the rows itself);
+ * M * K + 4 * M bytes for other M <= 16 (int8 codes and scales); for M > 16
+ * 2 * M * K + 4 * M + 4 * M bytes (fp16 codes, scales, per-token code sums).
+ * A problem that needs more returns CIDER_ERR_INVALID_ARGUMENT before the
+ * device is touched (for K = 2560: M above 6543).  The work-split buffers of
+ * the small-M K slices and of the per-channel GEMM's K pieces are used when
+ * they fit beside that, and left out otherwise (then whole row blocks / whole
+ * output tiles per CTA: the same results, possibly slower).
  *   - No cudaMalloc, cudaFree or other allocating call is made.
  *   - The first call on each device looks up the array's device address (a
  *     runtime call); make that first call before any stream capture.

@@ -93,15 +93,29 @@ def f16_bits(x: np.ndarray) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- a1
-def quantize_act(x_f16: np.ndarray):
+def quantize_act(x_f16: np.ndarray, threads: int = 1):
     """Per-token symmetric INT8 quantization (Cider README, "Metal kernel
     pipeline": quantize_per_token; "Quantization": activations per token).
-    x fp16 [M,K] -> (qa int8 [M,K], sa fp32 [M])."""
+    x fp16 [M,K] -> (qa int8 [M,K], sa fp32 [M]).  Rows are independent, so
+    ``threads > 1`` runs disjoint row ranges of the same single-threaded C
+    code concurrently (ctypes releases the GIL)."""
     x = f16_bits(x_f16)
     M, K = x.shape
     qa = np.empty((M, K), np.int8)
     sa = np.empty((M,), np.float32)
-    _load().oracle_quantize_act(_ptr(x), M, K, _ptr(qa), _ptr(sa))
+    lib = _load()
+
+    def run(r0, r1):
+        r0, r1 = int(r0), int(r1)
+        lib.oracle_quantize_act(_ptr(x) + r0 * K * 2, r1 - r0, K, _ptr(qa) + r0 * K,
+                                _ptr(sa) + r0 * 4)
+
+    if threads <= 1 or M < 2:
+        run(0, M)
+    else:
+        bounds = np.linspace(0, M, min(threads, M) + 1).astype(int)
+        with ThreadPoolExecutor(len(bounds) - 1) as ex:
+            list(ex.map(lambda i: run(bounds[i], bounds[i + 1]), range(len(bounds) - 1)))
     return qa, sa
 
 

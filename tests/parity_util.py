@@ -51,3 +51,34 @@ def assert_bits_equal(a: np.ndarray, b: np.ndarray, what: str = ""):
         i = tuple(idx[0])
         raise AssertionError(f"{what}: {len(idx)} of {a.size} differ; first at {i}: "
                              f"got {a[i]}, want {b[i]}")
+
+
+# Every fp16 (amax, x) pair, for the exhaustive quantization tests.
+def positive_fp16() -> np.ndarray:
+    """All positive finite fp16 values in increasing order (31743 values:
+    the 1023 subnormals, then every normal up to 65504)."""
+    return np.arange(1, 0x7C00, dtype=np.uint16).view(np.float16)
+
+
+# Row layout of the exhaustive test: element 0 is the row's maximum a_i, then
+# J = 1023 pairs (+v, -v) of values v <= a_i, then one zero.  Amax i (the i-th
+# positive value) needs ceil((i + 1) / J) rows to hold all i + 1 values <= it.
+EXH_W = 2048
+EXH_J = (EXH_W - 2) // 2
+
+
+def exhaustive_rows(pos: np.ndarray, i0: int, i1: int) -> np.ndarray:
+    """The rows for amax indices [i0, i1) (zeros where a row has no more values)."""
+    idx = np.arange(i0, i1)
+    counts = (idx + EXH_J) // EXH_J                   # ceil((i + 1) / J)
+    amax_i = np.repeat(idx, counts)
+    first = np.repeat(np.cumsum(counts) - counts, counts)
+    r = np.arange(len(amax_i)) - first                  # row number within its amax
+    j = r[:, None] * EXH_J + np.arange(EXH_J)[None, :]
+    valid = j <= amax_i[:, None]
+    vals = np.where(valid, pos[np.minimum(j, len(pos) - 1)], np.float16(0))
+    x = np.zeros((len(amax_i), EXH_W), np.float16)
+    x[:, 0] = pos[amax_i]
+    x[:, 1:1 + 2 * EXH_J:2] = vals
+    x[:, 2:2 + 2 * EXH_J:2] = -vals
+    return x

@@ -301,3 +301,85 @@ def test_kernel_timing_inside_cuda_graph(cider):
     g.replay()
     n, ms = cider.cider_timing_end()
     assert n == 2 and 0.0 < ms < 100.0
+
+
+def _rows_with_l1(targets, K, rng):
+    """fp16 activation rows whose codes are exactly chosen: each row holds
+    127 (so s_a = 127 / 127 = 1 and q = x, integers exact in fp16) and has
+    sum_k |q| = target, all codes >= 0: floor(target / 127) codes of 127 and
+    one code of target % 127, at random positions."""
+    x = np.zeros((len(targets), K), np.float16)
+    for r, t in enumerate(targets):
+        n127, rem = divmod(int(t), 127)
+        assert n127 >= 1 and n127 + (rem > 0) <= K
+        cols = rng.permutation(K)[:n127 + 1]
+        x[r, cols[:n127]] = 127
+        if rem:
+            x[r, cols[n127]] = rem
+    return x
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_fast_tile_bound_at_its_limit(cider, bits):
+    """The per-channel kernel runs a 256-token tile as one fp32 accumulation
+    over all of K when every token satisfies qmax_w * sum_k |q_a| <= 2^23
+    (qmax_w = 127 for INT8, 8 for INT4), else as exact chunked passes.
+
+    Token tile 0: every row exactly at the limit sum |q_a| = floor(2^23 /
+    qmax_w) (fast tile), with a weight row of constant sign so the partial
+    sums climb to ~8.39e6.  Tile 1: the same plus one row at limit + 1 (the
+    whole tile must take the chunked path).  Tile 2 (ragged): rows whose
+    weight-row-0 sum is odd and above 2^24, which one fp32 accumulation cannot
+    represent, so only the chunked path gets them right.  Accumulators and y
+    bit for bit against the oracle."""
+    qmax = 127 if bits == 8 else 8
+    limit = (1 << 23) // qmax
+    # INT4 needs longer rows to reach its limit (2^20 / 127 codes of 127) and an odd
+    # weight (7) whose product sum passes 2^24
+    K = 2560 if bits == 8 else 20480
+    wbig = 127 if bits == 8 else 7
+    over = (1 << 24) // wbig + 1
+    over += 1 - over % 2                      # odd sum, odd weight: odd product sum > 2^24
+    assert wbig * over > (1 << 24) and (wbig * over) % 2 == 1
+    rng = np.random.default_rng(321)
+    t0 = [limit] * 256
+    t1 = [limit] * 255 + [limit + 1]
+    t2 = [over] * 60 + [limit] * 20
+    x = _rows_with_l1(t0 + t1 + t2, K, rng)
+    M, N = x.shape[0], 136
+    qa, sa = oracle.quantize_act(x)
+    assert np.all(sa == 1.0)
+    l1 = np.abs(qa.astype(np.int64)).sum(axis=1)
+    assert l1[:256].max() == limit and l1[256:512].max() == limit + 1 and l1[512] == over
+    lo, hi = (-127, 127) if bits == 8 else (-8, 7)
+    qw = rng.integers(lo, hi + 1, size=(N, K)).astype(np.int8)
+    qw[0] = wbig                              # sign-matched: partial sums climb monotonically
+    qw[1] = -wbig
+    qw[2] = lo
+    qw_dev = qw if bits == 8 else oracle.pack_int4(qw)
+    acc_ref = oracle.gemm_acc(qa, qw, 0)
+    assert acc_ref[0, 0, 0] == wbig * limit and acc_ref[512, 0, 0] == wbig * over
+    acc = run_acc(cider, qa, qw_dev, 0, bits)
+    assert_bits_equal(acc, acc_ref, f"bound acc bits={bits}")
+    sw = (rng.random((N, 1)) * 1e-4 + 1e-5).astype(np.float32)
+    y = run_linear(cider, x, qw_dev, sw, 0, bits)
+    assert_bits_equal(y, oracle.linear(x, qw, sw, 0, threads=8), f"bound y bits={bits}")
+
+
+def test_full_size_shared_activation_projection_set(cider):
+    """The Qwen3-2B-shaped Q / K / V projections at prefill M = 1334: one
+    activation quantization (cider_quantize_act) shared by the three
+    projections through cider_w8a8_linear_prequant, per channel; sampled rows
+    bit for bit against the oracle."""
+    M, hidden = 1334, 2048
+    x = inputs.activations(M, hidden, seed=0)
+    qa, sa = cider.cider_quantize_act(to_dev(x))
+    rng = np.random.default_rng(1334)
+    rows = sorted(set([0, M - 1, M // 2] + list(rng.integers(0, M, 6))))
+    for i, name in enumerate(("q", "k", "v")):
+        N, K = inputs.QWEN3_2B[name]
+        qw, sw = oracle.quantize_weight_int8(inputs.weights(N, K, seed=1 + 2 * i), 0)
+        y = to_host(cider.cider_w8a8_linear_prequant(qa, sa, to_dev(qw), to_dev(sw), 0))
+        assert y.shape == (M, N)
+        yref = oracle.linear(x, qw, sw, 0, rows=rows, threads=8)
+        assert_bits_equal(y[rows], yref, f"Qwen3-2B {name} projection rows")

@@ -6,7 +6,8 @@ import pytest
 import torch
 
 import oracle
-from tests.parity_util import assert_bits_equal, require_gpu, to_dev, to_host
+from tests.parity_util import (EXH_J, EXH_W, assert_bits_equal, exhaustive_rows,
+                               positive_fp16, require_gpu, to_dev, to_host)
 from w4a8_quantized_linear_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -75,27 +76,76 @@ def test_no_device_error_left(cider):
     assert cider.cider_check_device_error() == 0
 
 
-def _exhaustive_amax_values():
-    rng = np.random.default_rng(2024)
-    fixed = [65504.0, 1.0, 127.0, 3.140625, 0.0009765625, 2.0 ** -24 * 37, 2.0 ** -14, 1000.0,
-             0.0016956329345703125, 0.50732421875, 2.0 ** -24, 6.0e-5, 0.3333, 254.0, 8191.0]
-    allv = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16).view(np.float16)
-    pos = allv[np.isfinite(allv) & (allv > 0)]
-    return fixed + [float(v) for v in rng.choice(pos, 25, replace=False)]
+@pytest.mark.timeout(900)
+def test_quantize_act_every_fp16_amax_and_value(cider):
+    """Every positive finite fp16 amax (31743 values) with every finite fp16
+    value |x| <= amax of both signs: about 1e9 (amax, x) pairs, all quantized
+    by cider_quantize_act and compared bit for bit (codes and scales) with the
+    oracle.  This covers the kernels' reciprocal-and-FMA division for every
+    input an fp16 row can give it."""
+    import os
+    pos = positive_fp16()
+    threads = max(1, min(16, os.cpu_count() or 1))
+    n = len(pos)
+    # chunks of about 24k rows (96 MB of fp16) each
+    bounds = [0]
+    rows_so_far = 0
+    for i in range(n):
+        rows_so_far += (i + EXH_J) // EXH_J
+        if rows_so_far >= 24576:
+            bounds.append(i + 1)
+            rows_so_far = 0
+    if bounds[-1] != n:
+        bounds.append(n)
+    pairs = 0
+    for i0, i1 in zip(bounds[:-1], bounds[1:]):
+        x = exhaustive_rows(pos, i0, i1)
+        qa, sa = cider.cider_quantize_act(to_dev(x))
+        qref, sref = oracle.quantize_act(x, threads=threads)
+        assert_bits_equal(to_host(sa).view(np.uint32), sref.view(np.uint32),
+                          f"s_a, amax {float(pos[i0])}..{float(pos[i1 - 1])}")
+        assert_bits_equal(to_host(qa), qref, f"q_a, amax {float(pos[i0])}..{float(pos[i1 - 1])}")
+        pairs += int(sum(2 * (i + 1) for i in range(i0, i1)))
+    assert pairs > 1_000_000_000
 
 
-@pytest.mark.parametrize("amax", _exhaustive_amax_values())
-def test_quantize_act_exhaustive_fp16_values(cider, amax):
-    """Every finite fp16 value |x| <= amax, in rows whose maximum is amax: codes
-    and scales bit-exact against the oracle (exercises the division, rounding
-    and clamp for all inputs a scale can see)."""
-    allv = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16).view(np.float16)
-    vals = allv[np.isfinite(allv) & (np.abs(allv.astype(np.float64)) <= amax)]
-    W = 2048
-    pad = (-len(vals)) % (W - 1)
-    vals = np.concatenate([vals, np.zeros(pad, np.float16)]).reshape(-1, W - 1)
-    x = np.concatenate([np.full((vals.shape[0], 1), amax, np.float16), vals], axis=1)
-    qa, sa = cider.cider_quantize_act(to_dev(x))
-    qref, sref = oracle.quantize_act(x)
-    assert_bits_equal(to_host(sa).view(np.uint32), sref.view(np.uint32), "s_a")
-    assert_bits_equal(to_host(qa), qref, "q_a")
+def _sampled_amax_indices(count: int) -> np.ndarray:
+    """Amax indices for the GEMV checks: the extremes, the subnormal /
+    normal boundary, every power of two, and a seeded random sample."""
+    pos = positive_fp16()
+    fixed = {0, 1, 2, 1022, 1023, 1024, len(pos) - 1}
+    fixed |= set(np.nonzero((pos.view(np.uint16) & 0x03FF) == 0)[0].tolist())   # powers of two
+    rng = np.random.default_rng(2025)
+    rest = rng.choice(len(pos), count - len(fixed), replace=False)
+    return np.array(sorted(fixed | set(rest.tolist())))
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_fused_gemv_quantization_sampled_fp16_values(cider, M):
+    """The small-M GEMV quantizes the rows itself for one token (dp4a form)
+    and for M * K <= 8192 (tensor-core form at M = 4).  Its codes are read
+    back through selector weights (weight row n holds a single 1 at column n,
+    so acc[m, n] = q_a[m, n]) and a power-of-two weight scale that keeps every
+    product in the fp16 normal range, where distinct codes give distinct y:
+    y must equal the oracle's dequantization of the oracle's codes, bit for
+    bit, for every value |x| <= amax of about 600 amax values."""
+    K = EXH_W
+    pos = positive_fp16()
+    idx = _sampled_amax_indices(600)
+    rows = np.concatenate([exhaustive_rows(pos, i, i + 1) for i in idx])
+    pad = (-len(rows)) % M
+    rows = np.concatenate([rows, np.zeros((pad, K), np.float16)])
+    sel = torch.eye(K, dtype=torch.int8, device="cuda")
+    qref, sref = oracle.quantize_act(rows, threads=8)
+    for r0 in range(0, len(rows), M):
+        x = rows[r0:r0 + M]
+        amax = float(np.abs(x.astype(np.float32)).max())
+        # 2^e with amax * 2^e in [512, 1024): every |y| <= 127 s_a 2^e < 1024 and,
+        # for nonzero codes, |y| >= s_a 2^e >= 4 (rows of one call share their amax
+        # up to a factor 2^10 here, far inside the fp16 normal range)
+        e = int(np.floor(np.log2(1024.0 / amax))) if amax > 0 else 0
+        sw = np.full((K, 1), np.float32(2.0 ** e), np.float32)
+        y = to_host(cider.cider_w8a8_linear(to_dev(x), sel, to_dev(sw), 0))
+        acc = qref[r0:r0 + M].astype(np.int32)
+        want = oracle.dequant_pc(acc, sref[r0:r0 + M], sw)
+        assert_bits_equal(y, want, f"fused GEMV M={M}, rows {r0}..{r0 + M - 1}, amax {amax}")

@@ -2,11 +2,13 @@
 not allocate device memory while they run (an engine that reserved almost all
 of HBM up front, or a decode loop that cannot let a memory pool grow).
 
-It uses one fixed scratch array in device memory instead of the library's
-memory pool, so its results must be the same as those of cider_w8a8_linear,
-call after call, even though every call reuses (and overwrites) that array.
-This file is collected last so that a stop-at-first-failure run has already
-run every other test before it.
+It runs the same dispatch and kernels as cider_w8a8_linear but takes its
+scratch from one fixed array in device memory, which every call reuses and
+overwrites.  So its results are checked against the oracle itself (per
+channel bit for bit, per group within the fp16 tolerance), on two calls in a
+row with different inputs, and against cider_w8a8_linear bit for bit.  This
+file is collected last so that a stop-at-first-failure run has already run
+every other test before it.
 """
 import ctypes
 
@@ -14,7 +16,8 @@ import numpy as np
 import pytest
 import torch
 
-from tests.parity_util import assert_fp16_close, require_gpu, to_host
+import oracle
+from tests.parity_util import assert_bits_equal, assert_fp16_close, require_gpu, to_host
 from w4a8_quantized_linear_gb300 import _build, inputs
 
 SCRATCH_BYTES = 32 * 1024 * 1024
@@ -32,27 +35,43 @@ def noalloc_entry(lib):
 @pytest.mark.parametrize("M,N,K,gs", [
     (200, 264, 1024, 0),      # tensor-core path, per channel
     (300, 136, 2048, 128),    # tensor-core path, per group
-    (3, 136, 2560, 64),       # small-M path, per group
+    (3, 136, 2560, 64),       # small M, rows quantized inside the GEMV (M * K <= 8192)
+    (2, 264, 10240, 0),       # small M, dp4a form, rows quantized first (M * K > 8192)
+    (2, 264, 10240, 128),
+    (16, 520, 2560, 0),       # small M, tensor-core form, rows quantized first
+    (16, 520, 2560, 64),
+    (1, 520, 12288, 128),     # one token, long rows
     (4096, 10240, 2560, 0),   # the benchmark workload (needs 21 MB of the 32 MiB array)
 ])
-def test_noalloc_matches_pooled_entry_on_consecutive_calls(M, N, K, gs):
+def test_noalloc_matches_oracle_on_consecutive_calls(M, N, K, gs):
     cider = require_gpu()
     f = noalloc_entry(cider.library())
     dev = torch.device("cuda")
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    W = torch.from_numpy(inputs.weights(N, K, seed=N + K)).to(dev)
-    qw, sw = cider.cider_quantize_weight_int8(W, gs)
+    W = inputs.weights(N, K, seed=N + K)
+    qw_h, sw_h = oracle.quantize_weight_int8(W, gs)
+    qw, sw = torch.from_numpy(qw_h).to(dev), torch.from_numpy(sw_h).to(dev)
     gran = cider.CIDER_PER_GROUP if gs else cider.CIDER_PER_CHANNEL
-    xs = [torch.from_numpy(inputs.activations(M, K, seed=40 + i)).to(dev) for i in range(2)]
+    xs_h = [inputs.activations(M, K, seed=40 + i) for i in range(2)]
+    xs = [torch.from_numpy(x).to(dev) for x in xs_h]
     ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for _ in range(2)]
     # two calls in a row through the C ABI; the second reuses the same scratch
     for x, y in zip(xs, ys):
         st = f(x.data_ptr(), M, N, K, qw.data_ptr(), sw.data_ptr(), gran, gs, y.data_ptr(), stream)
         assert st == 0, cider.library().cider_status_string(st)
     torch.cuda.synchronize()
-    for x, y in zip(xs, ys):
-        want = cider.cider_w8a8_linear(x, qw, sw, gs)
-        assert_fp16_close(to_host(y), to_host(want), f"noalloc M={M} N={N} K={K} gs={gs}")
+    full = M * N * K <= 2 ** 31
+    rows = np.arange(M) if full else np.array(sorted({0, 1, M // 2, M - 2, M - 1, 1234, 3001}))
+    for i, (xh, x, y) in enumerate(zip(xs_h, xs, ys)):
+        got = to_host(y)[rows]
+        want = oracle.linear(xh, qw_h, sw_h, gs, rows=rows, threads=8)
+        what = f"noalloc call {i} M={M} N={N} K={K} gs={gs}"
+        if gs == 0:
+            assert_bits_equal(got, want, what)
+        else:
+            assert_fp16_close(got, want, what)
+        # and the same bits as the pooled entry point (same kernels, same dispatch)
+        assert_bits_equal(got, to_host(cider.cider_w8a8_linear(x, qw, sw, gs))[rows], what + " vs pooled")
     assert cider.cider_check_device_error() == 0
 
 

@@ -34,33 +34,6 @@ bool force_unsupported() {
   return v != nullptr && v[0] == '1';
 }
 
-// Supported = compute capability 10.3 (GB300).  Caches the SM count.
-cider_status_t check_device(int* dev_out, int* num_sms) {
-  if (force_unsupported()) return CIDER_ERR_UNSUPPORTED_DEVICE;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    cudaGetLastError();
-    return CIDER_ERR_UNSUPPORTED_DEVICE;
-  }
-  DeviceInfo& d = g_dev[dev];
-  int st = d.state.load(std::memory_order_acquire);
-  if (st == 0) {
-    int major = 0, minor = 0, sms = 0;
-    bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
-              cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
-              cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
-    if (!ok) cudaGetLastError();
-    ok = ok && major == 10 && minor == 3 && sms > 0;
-    d.num_sms = sms;
-    st = ok ? 1 : 2;
-    d.state.store(st, std::memory_order_release);
-  }
-  if (st != 1) return CIDER_ERR_UNSUPPORTED_DEVICE;
-  if (dev_out) *dev_out = dev;
-  if (num_sms) *num_sms = d.num_sms;
-  return CIDER_OK;
-}
-
 cudaError_t get_pool(int dev, cudaMemPool_t* pool) {
   std::lock_guard<std::mutex> lk(g_pool_mu);
   if (!g_pool[dev]) {
@@ -83,23 +56,6 @@ cudaError_t get_pool(int dev, cudaMemPool_t* pool) {
   }
   *pool = g_pool[dev];
   return cudaSuccess;
-}
-
-// Scratch for one call, allocated and freed in stream order.
-struct Scratch {
-  void* ptr = nullptr;
-  cudaStream_t st = nullptr;
-  ~Scratch() {
-    if (ptr) cudaFreeAsync(ptr, st);
-  }
-};
-
-cudaError_t scratch_alloc(Scratch& s, int dev, size_t bytes, cudaStream_t st) {
-  cudaMemPool_t pool;
-  cudaError_t e = get_pool(dev, &pool);
-  if (e != cudaSuccess) return e;
-  s.st = st;
-  return cudaMallocFromPoolAsync(&s.ptr, bytes, pool, st);
 }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -169,124 +125,6 @@ cudaError_t timed_launch(cudaStream_t st, F&& launch) {
   return cudaSuccess;
 }
 
-struct LinearArgs {
-  const void* x = nullptr;  // fp16 / bf16 activations (or null for the prequant forms)
-  bool x_bf16 = false;
-  const int8_t* qa = nullptr;
-  const float* sa = nullptr;
-  int64_t M = 0, N = 0, K = 0;
-  const void* w = nullptr;
-  bool int4 = false;
-  const float* sw = nullptr;
-  int granularity = 0, group_size = 0;
-  void* y = nullptr;
-  int32_t* acc = nullptr;
-  int mode = cider::kEpiY;
-  cudaStream_t st = nullptr;
-};
-
-cider_status_t validate_linear(const LinearArgs& a) {
-  if (a.M < 0 || a.N < 0 || a.K < 0) return CIDER_ERR_INVALID_ARGUMENT;
-  if (a.M > kMaxDim || a.N > kMaxDim) return CIDER_ERR_INVALID_ARGUMENT;
-  const bool prequant = a.x == nullptr;
-  if (prequant ? (!a.qa || (a.mode == cider::kEpiY && !a.sa)) : false)
-    return CIDER_ERR_INVALID_ARGUMENT;
-  if (!a.w) return CIDER_ERR_INVALID_ARGUMENT;
-  if (a.mode == cider::kEpiY && (!a.sw || !a.y)) return CIDER_ERR_INVALID_ARGUMENT;
-  if (a.mode == cider::kEpiAcc && !a.acc) return CIDER_ERR_INVALID_ARGUMENT;
-  if (!valid_k(a.K) || a.N % 8 != 0) return CIDER_ERR_INVALID_ARGUMENT;
-  if (a.mode == cider::kEpiY) {
-    if (!valid_grouping(a.granularity, a.group_size, a.K)) return CIDER_ERR_INVALID_ARGUMENT;
-  } else {
-    if (!(a.group_size == 0 || ((a.group_size == 64 || a.group_size == 128) && a.K % a.group_size == 0)))
-      return CIDER_ERR_INVALID_ARGUMENT;
-  }
-  if ((a.x && !aligned(a.x, 16)) || (a.qa && !aligned(a.qa, 16)) || !aligned(a.w, 16) ||
-      (a.y && !aligned(a.y, 16)))
-    return CIDER_ERR_MISALIGNED;
-  if ((a.sa && !aligned(a.sa, 4)) || (a.sw && !aligned(a.sw, 4)) || (a.acc && !aligned(a.acc, 4)))
-    return CIDER_ERR_MISALIGNED;
-  return CIDER_OK;
-}
-
-cider_status_t run_linear(const LinearArgs& a) {
-  if (a.M == 0 || a.N == 0) return CIDER_OK;
-  cider_status_t s = validate_linear(a);
-  if (s != CIDER_OK) return s;
-  int dev = 0, sms = 0;
-  s = check_device(&dev, &sms);
-  if (s != CIDER_OK) return s;
-  const uint8_t* w = static_cast<const uint8_t*>(a.w);
-  __half* y = static_cast<__half*>(a.y);
-  const int gs = a.group_size;
-  Scratch scratch;
-  if (cider::gemv_fits(a.M, a.K)) {
-    // small M: for one token or short rows the GEMV quantizes the rows itself
-    // (every CTA repeats that work, cheaper than a second launch for so few
-    // values); otherwise one quantization kernel writes the int8 codes first.
-    // bf16 rows, and problems whose K is split over several CTAs per row
-    // block, always take the quantization kernel.
-    const size_t pbytes = cider::gemv_part_bytes(a.M, a.N, a.K, a.int4, gs, a.mode, sms);
-    const __half* xg = static_cast<const __half*>(a.x);
-    const int8_t* qa = a.qa;
-    const float* sa = a.sa;
-    void* part = nullptr;
-    const bool quantize_first =
-        a.x && (a.x_bf16 || pbytes > 0 || !cider::gemv_quantizes_itself(a.M, a.K));
-    const size_t qbytes = quantize_first ? round_up(static_cast<size_t>(a.M * a.K), 256) : 0;
-    const size_t sbytes = quantize_first ? round_up(4 * a.M, 256) : 0;
-    if (qbytes + sbytes + pbytes > 0) {
-      cudaError_t e = scratch_alloc(scratch, dev, qbytes + sbytes + round_up(pbytes, 256), a.st);
-      if (e != cudaSuccess) return cuda_status(e);
-      uint8_t* base = static_cast<uint8_t*>(scratch.ptr);
-      if (pbytes > 0) part = base + qbytes + sbytes;
-      if (quantize_first) {
-        int8_t* qs = reinterpret_cast<int8_t*>(base);
-        float* ss = reinterpret_cast<float*>(base + qbytes);
-        e = a.x_bf16 ? cider::launch_quant_act_s8_bf16(static_cast<const __nv_bfloat16*>(a.x), a.M,
-                                                       a.K, qs, ss, a.st)
-                     : cider::launch_quant_act_s8(xg, a.M, a.K, qs, ss, a.st);
-        if (e != cudaSuccess) return cuda_status(e);
-        xg = nullptr;
-        qa = qs;
-        sa = ss;
-      }
-    }
-    return cuda_status(timed_launch(a.st, [&] {
-      return cider::launch_gemv(xg, qa, sa, a.M, a.N, a.K, w, a.int4, a.sw, gs, a.mode, y, a.acc,
-                                part, sms, a.st);
-    }));
-  }
-  // tensor-core path: activation codes as fp16 integers, scales, row sums of |code|
-  const size_t qbytes = round_up(static_cast<size_t>(a.M * a.K) * 2, 256);
-  const size_t vbytes = round_up(4 * a.M, 256);
-  const cider::GemmScratch gsc = cider::gemm_tc_scratch(a.M, a.N, a.K, gs);
-  cudaError_t e = scratch_alloc(scratch, dev, qbytes + 2 * vbytes + gsc.bytes, a.st);
-  if (e != cudaSuccess) return cuda_status(e);
-  uint8_t* sbase = static_cast<uint8_t*>(scratch.ptr);
-  __half* q16 = reinterpret_cast<__half*>(sbase);
-  int* row_l1 = reinterpret_cast<int*>(sbase + qbytes + vbytes);
-  uint8_t* ws = gsc.bytes ? sbase + qbytes + 2 * vbytes : nullptr;
-  int* zero = ws ? reinterpret_cast<int*>(ws + gsc.zero_offset) : nullptr;
-  const float* sa = a.sa;
-  if (a.x) {
-    float* sscr = reinterpret_cast<float*>(sbase + qbytes);
-    e = a.x_bf16 ? cider::launch_quant_act_f16_from_bf16(static_cast<const __nv_bfloat16*>(a.x),
-                                                         a.M, a.K, q16, sscr, row_l1, zero,
-                                                         gsc.zero_words, a.st)
-                 : cider::launch_quant_act_f16(static_cast<const __half*>(a.x), a.M, a.K, q16, sscr,
-                                               row_l1, zero, gsc.zero_words, a.st);
-    sa = sscr;
-  } else {
-    e = cider::launch_codes_s8_to_f16(a.qa, a.M, a.K, q16, row_l1, zero, gsc.zero_words, a.st);
-  }
-  if (e != cudaSuccess) return cuda_status(e);
-  return cuda_status(timed_launch(a.st, [&] {
-    return cider::launch_gemm_tc(q16, sa, row_l1, a.M, a.N, a.K, w, a.int4, a.sw, gs, a.mode, y,
-                                 a.acc, ws, sms, a.st);
-  }));
-}
-
 template <typename F>
 cider_status_t guarded(F&& f) {
   try {
@@ -304,7 +142,7 @@ cider_status_t quantize_weight(const float* w, int64_t N, int64_t K, int group_s
     return CIDER_ERR_INVALID_ARGUMENT;
   if (!aligned(w, 16) || !aligned(q, 16)) return CIDER_ERR_MISALIGNED;
   if (!aligned(sw, 4)) return CIDER_ERR_MISALIGNED;
-  cider_status_t s = check_device(nullptr, nullptr);
+  cider_status_t s = cider::check_device(nullptr, nullptr);
   if (s != CIDER_OK) return s;
   return cuda_status(cider::launch_quant_weight(w, N, K, group_size, int4,
                                                 static_cast<uint8_t*>(q), sw,
@@ -313,11 +151,191 @@ cider_status_t quantize_weight(const float* w, int64_t N, int64_t K, int group_s
 
 }  // namespace
 
+namespace cider {
+
+// Supported = compute capability 10.3 (GB300).  Caches the SM count.
+cider_status_t check_device(int* dev_out, int* num_sms) {
+  if (force_unsupported()) return CIDER_ERR_UNSUPPORTED_DEVICE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return CIDER_ERR_UNSUPPORTED_DEVICE;
+  }
+  DeviceInfo& d = g_dev[dev];
+  int st = d.state.load(std::memory_order_acquire);
+  if (st == 0) {
+    int major = 0, minor = 0, sms = 0;
+    bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+              cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+              cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
+    if (!ok) cudaGetLastError();
+    ok = ok && major == 10 && minor == 3 && sms > 0;
+    d.num_sms = sms;
+    st = ok ? 1 : 2;
+    d.state.store(st, std::memory_order_release);
+  }
+  if (st != 1) return CIDER_ERR_UNSUPPORTED_DEVICE;
+  if (dev_out) *dev_out = dev;
+  if (num_sms) *num_sms = d.num_sms;
+  return CIDER_OK;
+}
+
+ScratchSource::ScratchSource(ScratchSource&& o) noexcept
+    : st_(o.st_), base_(o.base_), capacity_(o.capacity_), pool_ptr_(o.pool_ptr_) {
+  o.pool_ptr_ = nullptr;
+}
+
+ScratchSource::~ScratchSource() {
+  if (pool_ptr_) cudaFreeAsync(pool_ptr_, st_);
+}
+
+cider_status_t ScratchSource::get(size_t bytes, void** out) {
+  if (base_ != nullptr) {
+    if (bytes > capacity_) return CIDER_ERR_INVALID_ARGUMENT;
+    *out = base_;
+    return CIDER_OK;
+  }
+  if (pool_ptr_ != nullptr) return CIDER_ERR_INVALID_ARGUMENT;   // one request per call
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cuda_status(cudaErrorInvalidDevice);
+  cudaMemPool_t pool;
+  e = get_pool(dev, &pool);
+  if (e == cudaSuccess) e = cudaMallocFromPoolAsync(&pool_ptr_, bytes, pool, st_);
+  if (e != cudaSuccess) {
+    pool_ptr_ = nullptr;
+    return cuda_status(e);
+  }
+  *out = pool_ptr_;
+  return CIDER_OK;
+}
+
+cider_status_t validate_linear(const LinearArgs& a) {
+  if (a.M < 0 || a.N < 0 || a.K < 0) return CIDER_ERR_INVALID_ARGUMENT;
+  if (a.M > kMaxDim || a.N > kMaxDim) return CIDER_ERR_INVALID_ARGUMENT;
+  const bool prequant = a.x == nullptr;
+  if (prequant ? (!a.qa || (a.mode == kEpiY && !a.sa)) : false)
+    return CIDER_ERR_INVALID_ARGUMENT;
+  if (!a.w) return CIDER_ERR_INVALID_ARGUMENT;
+  if (a.mode == kEpiY && (!a.sw || !a.y)) return CIDER_ERR_INVALID_ARGUMENT;
+  if (a.mode == kEpiAcc && !a.acc) return CIDER_ERR_INVALID_ARGUMENT;
+  if (!valid_k(a.K) || a.N % 8 != 0) return CIDER_ERR_INVALID_ARGUMENT;
+  if (a.mode == kEpiY) {
+    if (!valid_grouping(a.granularity, a.group_size, a.K)) return CIDER_ERR_INVALID_ARGUMENT;
+  } else {
+    if (!(a.group_size == 0 || ((a.group_size == 64 || a.group_size == 128) && a.K % a.group_size == 0)))
+      return CIDER_ERR_INVALID_ARGUMENT;
+  }
+  if ((a.x && !aligned(a.x, 16)) || (a.qa && !aligned(a.qa, 16)) || !aligned(a.w, 16) ||
+      (a.y && !aligned(a.y, 16)))
+    return CIDER_ERR_MISALIGNED;
+  if ((a.sa && !aligned(a.sa, 4)) || (a.sw && !aligned(a.sw, 4)) || (a.acc && !aligned(a.acc, 4)))
+    return CIDER_ERR_MISALIGNED;
+  return CIDER_OK;
+}
+
+size_t linear_required_scratch(const LinearArgs& a) {
+  if (a.M <= 0 || a.N <= 0 || a.K <= 0) return 0;
+  if (gemv_fits(a.M, a.K)) {
+    const bool quantize_first = a.x && (a.x_bf16 || !gemv_quantizes_itself(a.M, a.K));
+    return quantize_first ? round_up(static_cast<size_t>(a.M * a.K), 256) + round_up(4 * a.M, 256)
+                          : 0;
+  }
+  return round_up(static_cast<size_t>(a.M * a.K) * 2, 256) + 2 * round_up(4 * a.M, 256);
+}
+
+cider_status_t run_linear(const LinearArgs& a, ScratchSource& scratch) {
+  if (a.M == 0 || a.N == 0) return CIDER_OK;
+  cider_status_t s = validate_linear(a);
+  if (s != CIDER_OK) return s;
+  int dev = 0, sms = 0;
+  s = check_device(&dev, &sms);
+  if (s != CIDER_OK) return s;
+  const uint8_t* w = static_cast<const uint8_t*>(a.w);
+  __half* y = static_cast<__half*>(a.y);
+  const int gs = a.group_size;
+  if (gemv_fits(a.M, a.K)) {
+    // small M: for one token or short rows the GEMV quantizes the rows itself
+    // (every CTA repeats that work, cheaper than a second launch for so few
+    // values); otherwise one quantization kernel writes the int8 codes first.
+    // bf16 rows, and problems whose K is split over several CTAs per row
+    // block, always take the quantization kernel.  The K split's partial sums
+    // are optional scratch: without room for them the row blocks stay whole.
+    const size_t qs_bytes = round_up(static_cast<size_t>(a.M * a.K), 256) + round_up(4 * a.M, 256);
+    size_t pbytes = gemv_part_bytes(a.M, a.N, a.K, a.int4, gs, a.mode, sms);
+    if (pbytes > 0 && !scratch.fits((a.x ? qs_bytes : 0) + round_up(pbytes, 256))) pbytes = 0;
+    const __half* xg = static_cast<const __half*>(a.x);
+    const int8_t* qa = a.qa;
+    const float* sa = a.sa;
+    void* part = nullptr;
+    const bool quantize_first =
+        a.x && (a.x_bf16 || pbytes > 0 || !gemv_quantizes_itself(a.M, a.K));
+    const size_t qbytes = quantize_first ? round_up(static_cast<size_t>(a.M * a.K), 256) : 0;
+    const size_t sbytes = quantize_first ? round_up(4 * a.M, 256) : 0;
+    if (qbytes + sbytes + pbytes > 0) {
+      void* sp = nullptr;
+      s = scratch.get(qbytes + sbytes + round_up(pbytes, 256), &sp);
+      if (s != CIDER_OK) return s;
+      uint8_t* base = static_cast<uint8_t*>(sp);
+      if (pbytes > 0) part = base + qbytes + sbytes;
+      if (quantize_first) {
+        int8_t* qs = reinterpret_cast<int8_t*>(base);
+        float* ss = reinterpret_cast<float*>(base + qbytes);
+        cudaError_t e = a.x_bf16 ? launch_quant_act_s8_bf16(static_cast<const __nv_bfloat16*>(a.x),
+                                                            a.M, a.K, qs, ss, a.st)
+                                 : launch_quant_act_s8(xg, a.M, a.K, qs, ss, a.st);
+        if (e != cudaSuccess) return cuda_status(e);
+        xg = nullptr;
+        qa = qs;
+        sa = ss;
+      }
+    }
+    return cuda_status(timed_launch(a.st, [&] {
+      return launch_gemv(xg, qa, sa, a.M, a.N, a.K, w, a.int4, a.sw, gs, a.mode, y, a.acc, part,
+                         sms, a.st);
+    }));
+  }
+  // tensor-core path: activation codes as fp16 integers, scales, row sums of
+  // |code|; the per-channel GEMM's K-piece workspace is optional scratch
+  // (without it every output tile is computed whole by one CTA pair)
+  const size_t qbytes = round_up(static_cast<size_t>(a.M * a.K) * 2, 256);
+  const size_t vbytes = round_up(4 * a.M, 256);
+  GemmScratch gsc = gemm_tc_scratch(a.M, a.N, a.K, gs);
+  if (gsc.bytes > 0 && !scratch.fits(qbytes + 2 * vbytes + gsc.bytes)) gsc = GemmScratch{};
+  void* sp = nullptr;
+  s = scratch.get(qbytes + 2 * vbytes + gsc.bytes, &sp);
+  if (s != CIDER_OK) return s;
+  uint8_t* sbase = static_cast<uint8_t*>(sp);
+  __half* q16 = reinterpret_cast<__half*>(sbase);
+  int* row_l1 = reinterpret_cast<int*>(sbase + qbytes + vbytes);
+  uint8_t* ws = gsc.bytes ? sbase + qbytes + 2 * vbytes : nullptr;
+  int* zero = ws ? reinterpret_cast<int*>(ws + gsc.zero_offset) : nullptr;
+  const float* sa = a.sa;
+  cudaError_t e;
+  if (a.x) {
+    float* sscr = reinterpret_cast<float*>(sbase + qbytes);
+    e = a.x_bf16 ? launch_quant_act_f16_from_bf16(static_cast<const __nv_bfloat16*>(a.x), a.M, a.K,
+                                                  q16, sscr, row_l1, zero, gsc.zero_words, a.st)
+                 : launch_quant_act_f16(static_cast<const __half*>(a.x), a.M, a.K, q16, sscr,
+                                        row_l1, zero, gsc.zero_words, a.st);
+    sa = sscr;
+  } else {
+    e = launch_codes_s8_to_f16(a.qa, a.M, a.K, q16, row_l1, zero, gsc.zero_words, a.st);
+  }
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(timed_launch(a.st, [&] {
+    return launch_gemm_tc(q16, sa, row_l1, a.M, a.N, a.K, w, a.int4, a.sw, gs, a.mode, y, a.acc,
+                          ws, sms, a.st);
+  }));
+}
+
+}  // namespace cider
+
 extern "C" {
 
 int cider_version(void) { return 100; }
 
-int cider_is_available(void) { return check_device(nullptr, nullptr) == CIDER_OK ? 1 : 0; }
+int cider_is_available(void) { return cider::check_device(nullptr, nullptr) == CIDER_OK ? 1 : 0; }
 
 const char* cider_status_string(int status) {
   switch (status) {
@@ -338,7 +356,7 @@ static cider_status_t quantize_act_entry(const void* x, bool bf16, int64_t M, in
     if (M < 0 || M > kMaxDim || !x || !qa || !sa || !valid_k(K)) return CIDER_ERR_INVALID_ARGUMENT;
     if (!aligned(x, 16) || !aligned(qa, 16)) return CIDER_ERR_MISALIGNED;
     if (!aligned(sa, 4)) return CIDER_ERR_MISALIGNED;
-    cider_status_t s = check_device(nullptr, nullptr);
+    cider_status_t s = cider::check_device(nullptr, nullptr);
     if (s != CIDER_OK) return s;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     return cuda_status(bf16 ? cider::launch_quant_act_s8_bf16(static_cast<const __nv_bfloat16*>(x),
@@ -364,7 +382,7 @@ cider_status_t cider_int4_from_offset_binary(const uint8_t* src, uint8_t* dst, i
     if (nbytes == 0) return CIDER_OK;
     if (nbytes < 0 || !src || !dst) return CIDER_ERR_INVALID_ARGUMENT;
     if (!aligned(src, 16) || !aligned(dst, 16)) return CIDER_ERR_MISALIGNED;
-    cider_status_t s = check_device(nullptr, nullptr);
+    cider_status_t s = cider::check_device(nullptr, nullptr);
     if (s != CIDER_OK) return s;
     return cuda_status(
         cider::launch_int4_from_offset(src, dst, nbytes, static_cast<cudaStream_t>(stream)));
@@ -386,7 +404,7 @@ static cider_status_t linear_entry(const void* x, const int8_t* qa, const float*
                                    int granularity, int group_size, void* y, void* stream,
                                    bool x_bf16 = false) {
   return guarded([&] {
-    LinearArgs a;
+    cider::LinearArgs a;
     a.x = x;
     a.x_bf16 = x_bf16;
     a.qa = qa;
@@ -404,7 +422,8 @@ static cider_status_t linear_entry(const void* x, const int8_t* qa, const float*
     a.st = static_cast<cudaStream_t>(stream);
     if (M == 0 || N == 0) return CIDER_OK;
     if (!x && !qa) return CIDER_ERR_INVALID_ARGUMENT;
-    return run_linear(a);
+    cider::ScratchSource scratch = cider::ScratchSource::pooled(a.st);
+    return cider::run_linear(a, scratch);
   });
 }
 
@@ -458,7 +477,7 @@ static cider_status_t acc_entry(const int8_t* qa, int64_t M, int64_t N, int64_t 
                                 bool int4, int group_size, int32_t* acc, void* stream) {
   return guarded([&] {
     if (M != 0 && N != 0 && !qa) return CIDER_ERR_INVALID_ARGUMENT;
-    LinearArgs a;
+    cider::LinearArgs a;
     a.qa = qa;
     a.M = M;
     a.N = N;
@@ -469,7 +488,8 @@ static cider_status_t acc_entry(const int8_t* qa, int64_t M, int64_t N, int64_t 
     a.acc = acc;
     a.mode = cider::kEpiAcc;
     a.st = static_cast<cudaStream_t>(stream);
-    return run_linear(a);
+    cider::ScratchSource scratch = cider::ScratchSource::pooled(a.st);
+    return cider::run_linear(a, scratch);
   });
 }
 
@@ -525,7 +545,7 @@ cider_status_t cider_timing_end(int64_t* count, double* total_ms) {
 
 cider_status_t cider_check_device_error(void* stream) {
   return guarded([&] {
-    cider_status_t s = check_device(nullptr, nullptr);
+    cider_status_t s = cider::check_device(nullptr, nullptr);
     if (s != CIDER_OK) return s;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return cuda_status(cudaErrorUnknown);
@@ -538,7 +558,7 @@ cider_status_t cider_check_device_error(void* stream) {
 cider_status_t cider_debug_wait_timeout(int64_t max_polls, void* stream) {
   return guarded([&] {
     if (max_polls < 1) return CIDER_ERR_INVALID_ARGUMENT;
-    cider_status_t s = check_device(nullptr, nullptr);
+    cider_status_t s = cider::check_device(nullptr, nullptr);
     if (s != CIDER_OK) return s;
     return cuda_status(cider::launch_debug_wait_timeout(max_polls, static_cast<cudaStream_t>(stream)));
   });

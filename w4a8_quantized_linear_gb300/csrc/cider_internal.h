@@ -11,6 +11,8 @@
 
 #include <atomic>
 
+#include "cider.h"
+
 namespace cider {
 
 // 2D TMA tensor map over a row-major matrix: `inner` elements per row,
@@ -112,5 +114,67 @@ cudaError_t read_and_clear_device_error(int* value);
 cudaError_t device_error_word(int** ptr);
 constexpr uint64_t kKernelWaitTimeoutNs = 2000000000ull;
 cudaError_t launch_debug_wait_timeout(int64_t max_polls, cudaStream_t st);
+
+// ---------------------------------------------------------------- cider_api.cu
+// One linear / accumulator call, as the C entry points receive it.
+struct LinearArgs {
+  const void* x = nullptr;  // fp16 / bf16 activations (or null for the prequant forms)
+  bool x_bf16 = false;
+  const int8_t* qa = nullptr;
+  const float* sa = nullptr;
+  int64_t M = 0, N = 0, K = 0;
+  const void* w = nullptr;
+  bool int4 = false;
+  const float* sw = nullptr;
+  int granularity = 0, group_size = 0;
+  void* y = nullptr;
+  int32_t* acc = nullptr;
+  int mode = kEpiY;
+  cudaStream_t st = nullptr;
+};
+
+// Host argument checks shared by every linear entry point (the order the
+// public header documents): sizes, pointers, K and N rules, grouping, alignment.
+cider_status_t validate_linear(const LinearArgs& a);
+// Current device is a supported sm_103 GPU (cached per device; honours
+// CIDER_FORCE_UNSUPPORTED=1); writes its index and SM count.
+cider_status_t check_device(int* dev_out, int* num_sms);
+
+// Where a call's scratch memory comes from: the library's per-device
+// stream-ordered pool (allocated and freed on the call's stream), or a fixed
+// caller-provided region [base, base + capacity) that is carved up without
+// any allocation.
+class ScratchSource {
+ public:
+  static ScratchSource pooled(cudaStream_t st) { return ScratchSource(st, nullptr, 0); }
+  static ScratchSource fixed(void* base, size_t capacity) {
+    return ScratchSource(nullptr, base, capacity);
+  }
+  ScratchSource(ScratchSource&& o) noexcept;
+  ScratchSource(const ScratchSource&) = delete;
+  ScratchSource& operator=(const ScratchSource&) = delete;
+  ~ScratchSource();
+  // Whether `bytes` can be had (always, for the pool).
+  bool fits(size_t bytes) const { return base_ == nullptr || bytes <= capacity_; }
+  // `bytes` of scratch for this call (at most one request per call): a pool
+  // allocation error maps to CIDER_ERR_CUDA, a fixed region too small to
+  // CIDER_ERR_INVALID_ARGUMENT.
+  cider_status_t get(size_t bytes, void** out);
+
+ private:
+  ScratchSource(cudaStream_t st, void* base, size_t cap) : st_(st), base_(base), capacity_(cap) {}
+  cudaStream_t st_;
+  void* base_;
+  size_t capacity_;
+  void* pool_ptr_ = nullptr;
+};
+
+// Scratch bytes a linear call cannot do without (activation codes and
+// per-token values; the K-piece and K-slice workspaces are optional and left
+// out when a fixed region has no room for them).
+size_t linear_required_scratch(const LinearArgs& a);
+// The M-bucket dispatch of every linear entry point: argument and device
+// checks, then the small-M GEMV (M <= 16) or quantization + tensor-core GEMM.
+cider_status_t run_linear(const LinearArgs& a, ScratchSource& scratch);
 
 }  // namespace cider
