@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libcider.so")
-SOURCES = ["cider_api.cu", "quant.cu", "gemv.cu", "gemm_tc.cu", "gemm_pair.cu", "noalloc.cu"]
+SOURCES = ["cider_api.cu", "quant.cu", "gemv.cu", "gemm_tc.cu", "gemm_pair.cu", "gemm_pg.cu", "noalloc.cu"]
 HEADERS = ["cider_device.cuh", "cider_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -109,6 +109,37 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// As mbar_wait_bounded, but each poll suspends the thread in hardware until
+// the phase completes or about `hint_ns` pass, so that waiting warps leave
+// the issue slots to the warps doing work (in kernels with many more waiting
+// warps than working ones).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_sleep_bounded(uint32_t bar, uint32_t parity,
+                                                   volatile uint32_t* abort_flag, int* err,
+                                                   uint64_t timeout_ns) {
+  if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      *abort_flag = 1u;
+      atomicOr(err, kDevErrTimeout);
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------- flags in global memory
 // A counter that other CTAs of the same launch wait on.  Every thread that
 // wrote data the waiters will read adds 1 with release semantics (covering
@@ -351,6 +382,22 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
 }
 
 // ---------------------------------------------------------------- loads
+// Asynchronous 4-byte global -> shared copy (completion tracked per thread by
+// commit groups); `valid` false writes zero and reads nothing.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(valid ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's most recent commit groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -101,6 +101,10 @@ cudaError_t launch_gemm_tc(const __half* qa16, const float* sa, const int* row_l
                            int64_t N, int64_t K, const uint8_t* w, bool int4, const float* sw,
                            int group_size, int mode, __half* y, int32_t* acc, void* workspace,
                            int num_sms, cudaStream_t st);
+// gemm_pg.cu: per-group tensor-core path on CTA pairs (see launch_gemm_tc).
+cudaError_t launch_gemm_pg(const __half* qa16, const float* sa, int64_t M, int64_t N, int64_t K,
+                           const uint8_t* w, bool int4, const float* sw, int group_size, int mode,
+                           __half* y, int32_t* acc, cudaStream_t st);
 // gemm_pair.cu: per-channel tensor-core path on CTA pairs (see launch_gemm_tc).
 GemmScratch gemm_pair_scratch(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_pair(const __half* qa16, const float* sa, const int* row_l1, int64_t M,

@@ -412,6 +412,10 @@ cudaError_t launch_gemm_tc(const __half* qa16, const float* sa, const int* row_l
                            int num_sms, cudaStream_t st) {
   if (group_size == 0)
     return launch_gemm_pair(qa16, sa, row_l1, M, N, K, w, int4, sw, mode, y, acc, workspace, st);
+  // 128-element groups: the CTA-pair kernel of gemm_pg.cu; 64-element groups
+  // (twice the drains per K) run faster on this file's single-CTA kernel
+  if (group_size == 128)
+    return launch_gemm_pg(qa16, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, st);
   CUtensorMap tmA, tmB;
   if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qa16, K, M, K * 2, kBK, kTileM,
                    CU_TENSOR_MAP_SWIZZLE_128B))
