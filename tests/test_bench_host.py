@@ -60,11 +60,25 @@ def test_clock_sampler_without_nvidia_smi(monkeypatch, tmp_path):
     assert c.stop() is None
 
 
-def test_traffic_attaches_to_the_kernels_own_sources(monkeypatch):
+def test_traffic_attaches_to_the_kernels_own_sources(monkeypatch, tmp_path):
+    """A traffic record is used only while the hash of the kernel's own
+    sources (comments ignored) matches the one it was taken on."""
+    import json
+    import shutil
     head = "W8A8 per-channel linear M=4096 N=10240 K=2560"
-    assert bench.ncu_traffic(head) is not None          # recorded on the current source
-    real = bench.kernel_source_sha
-    monkeypatch.setattr(bench, "kernel_source_sha", lambda names=(): real(names) + "x")
+    srcs = ["gemm_pair.cu", "cider_device.cuh"]
+    csrc = tmp_path / "w4a8_quantized_linear_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in srcs:
+        shutil.copy(os.path.join(bench.ROOT, "w4a8_quantized_linear_gb300", "csrc", f), csrc / f)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({head: {
+        "kernel_source_sha": bench.kernel_source_sha(tuple(srcs)), "sources": srcs,
+        "dram_bytes_per_launch": 123}}))
+    assert bench.ncu_traffic(head) == 123                 # recorded on the current source
+    with open(csrc / "gemm_pair.cu", "a") as f:
+        f.write("int one_more_line;\n")
     assert bench.ncu_traffic(head) is None                # any source change drops it
     assert bench.ncu_traffic("no such workload") is None
 
