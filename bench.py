@@ -173,7 +173,8 @@ def measured_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def kernel_source_sha(names=("gemm_pair.cu", "gemm_tc.cu", "gemv.cu", "cider_device.cuh")) -> str:
+def kernel_source_sha(names=("gemm_pair.cu", "gemm_pg.cu", "gemm_tc.cu", "gemv.cu",
+                             "cider_device.cuh")) -> str:
     """Hash of the kernels' CUDA sources with comments and blank lines removed,
     so that counters taken on a kernel stay attached to it until its code
     changes."""
@@ -211,7 +212,8 @@ def library_path(M: int, N: int, K: int, gs: int, bits: int = 8, num_sms: int = 
                 return "gemv_kernel (small-M weight-streaming GEMV, fused quantization)", 1
             return f"gemv_kernel (small-M weight-streaming GEMV, {form})", 2
     if gs:
-        return "gemm_tc_kernel (tcgen05 kind::f16 on exact integer codes, per-group epilogue)", 2
+        return ("gemm_pg_kernel (tcgen05 cta_group::2 on CTA pairs, 256x256 tiles, per-group drain "
+                "into fp32 running sums)"), 2
     return "gemm_pair_kernel (tcgen05 cta_group::2 on CTA pairs, 256x256 tiles)", 2
 
 
