@@ -59,8 +59,9 @@
 // of the tile's other pieces, adds up all s partials for its own 1/s of the
 // tile's weight rows (exact int32) and dequantizes and stores that part of
 // y.  Every pair writes before it waits, so the waits cannot cycle; the
-// pieces of a tile run at the same time on co-resident pairs (the grid never
-// exceeds the pairs the GPU holds at once).  The flags are zeroed by the
+// pieces of a tile run at the same time on co-resident pairs: such a launch
+// is cooperative (all pairs resident at once, or the launch fails) and never
+// exceeds the pairs the GPU holds at once.  The flags are zeroed by the
 // activation-quantization kernel that precedes every launch.
 //
 // Exactness per tile: every partial sum of token m is bounded by
@@ -737,6 +738,10 @@ PairPlan pair_plan(int64_t M, int64_t N, int64_t K, int nc, bool allow_sk) {
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
+// A launch whose cut tiles make pieces wait on each other is cooperative:
+// the runtime then starts it only with every CTA pair resident at once (or
+// fails the launch), so no piece can wait on a partner that other work on
+// the GPU keeps from starting.  The bounded waits stay as a backstop.
 template <bool INT4, int EPI>
 cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmW, const PairArgs& a,
                         int clusters, cudaStream_t st) {
@@ -746,8 +751,21 @@ cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmW, const Pa
   cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::kSmemBytes,
                                           attr_done);
   if (e != cudaSuccess) return e;
-  kern<<<2 * clusters, kPThreads, C::kSmemBytes, st>>>(tmX, tmW, a);
-  return cudaGetLastError();
+  if (a.sk_tiles == 0) {
+    kern<<<2 * clusters, kPThreads, C::kSmemBytes, st>>>(tmX, tmW, a);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+  cfg.blockDim = dim3(kPThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmX, tmW, a);
 }
 
 }  // namespace
