@@ -53,6 +53,15 @@ def _configure(lib):
     lib.oracle_f16_to_f32.restype = ctypes.c_float
     lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
     lib.oracle_f32_to_f16.restype = ctypes.c_uint16
+    lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_quantize_weight_int8_clip.argtypes = [p, i64, i64, i64, ctypes.c_double, p, p, p]
+    lib.oracle_quantize_weight_int4_clip.argtypes = [p, i64, i64, i64, ctypes.c_double, p, p, p]
+    lib.oracle_dequant_pc_bf16.argtypes = [p, p, p, i64, i64, p]
+    lib.oracle_dequant_pg_bf16.argtypes = [p, p, p, i64, i64, i64, p]
+    lib.oracle_linear_rows_ex.argtypes = [p, ctypes.c_int, i64, i64, p, p, i64, i64, i64, p, p,
+                                          ctypes.c_int, p]
+    lib.oracle_linear_rows_ex.restype = ctypes.c_int
     lib.oracle_quantize_act.argtypes = [p, i64, i64, p, p]
     lib.oracle_quantize_act_bf16.argtypes = [p, i64, i64, p, p]
     lib.oracle_int4_from_offset_binary.argtypes = [p, i64, p]
@@ -142,28 +151,40 @@ def int4_from_offset_binary(src: np.ndarray) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- a2 / a4
-def quantize_weight_int8(W: np.ndarray, group_size: int = 0):
-    """Symmetric min-max INT8 weights, per channel (group_size=0) or per group
-    (Cider README, "Quantization" and "W8A8 quantization granularity").
+def quantize_weight_int8(W: np.ndarray, group_size: int = 0, clip_percentile=None):
+    """Symmetric INT8 weights, per channel (group_size=0) or per group
+    (Cider README, "Quantization" and "W8A8 quantization granularity"), with
+    min-max scales or, given ``clip_percentile`` in (0, 100], percentile-clipped
+    ones ("Notes": clip_percentile=99.9; definition in cider_oracle.c).
     W fp32 [N,K] -> (qw int8 [N,K], sw fp32 [N,G])."""
     W = _c(W, np.float32)
     N, K = W.shape
     G = K // group_size if group_size else 1
     qw = np.empty((N, K), np.int8)
     sw = np.empty((N, G), np.float32)
-    _load().oracle_quantize_weight_int8(_ptr(W), N, K, group_size, _ptr(qw), _ptr(sw))
+    if clip_percentile is None:
+        _load().oracle_quantize_weight_int8(_ptr(W), N, K, group_size, _ptr(qw), _ptr(sw))
+    else:
+        tmp = np.empty((K,), np.float32)
+        _load().oracle_quantize_weight_int8_clip(_ptr(W), N, K, group_size, float(clip_percentile),
+                                                 _ptr(qw), _ptr(sw), _ptr(tmp))
     return qw, sw
 
 
-def quantize_weight_int4(W: np.ndarray, group_size: int = 0):
-    """Symmetric min-max INT4 weights in [-8,7] with s = max|W|/7.
-    W fp32 [N,K] -> (q4 int8 [N,K] values, sw fp32 [N,G])."""
+def quantize_weight_int4(W: np.ndarray, group_size: int = 0, clip_percentile=None):
+    """Symmetric INT4 weights in [-8,7] with s = max|W|/7 (or the clipped
+    percentile / 7).  W fp32 [N,K] -> (q4 int8 [N,K] values, sw fp32 [N,G])."""
     W = _c(W, np.float32)
     N, K = W.shape
     G = K // group_size if group_size else 1
     q4 = np.empty((N, K), np.int8)
     sw = np.empty((N, G), np.float32)
-    _load().oracle_quantize_weight_int4(_ptr(W), N, K, group_size, _ptr(q4), _ptr(sw))
+    if clip_percentile is None:
+        _load().oracle_quantize_weight_int4(_ptr(W), N, K, group_size, _ptr(q4), _ptr(sw))
+    else:
+        tmp = np.empty((K,), np.float32)
+        _load().oracle_quantize_weight_int4_clip(_ptr(W), N, K, group_size, float(clip_percentile),
+                                                 _ptr(q4), _ptr(sw), _ptr(tmp))
     return q4, sw
 
 
@@ -201,39 +222,44 @@ def gemm_acc(qa: np.ndarray, qw: np.ndarray, group_size: int = 0) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- a5
-def dequant_pc(acc: np.ndarray, sa: np.ndarray, sw: np.ndarray) -> np.ndarray:
-    """y = fp16((float(acc) * s_a) * s_w) (Cider README, "Quantization":
-    output dequant).  acc [M,N] or [M,N,1] -> fp16 [M,N]."""
+def dequant_pc(acc: np.ndarray, sa: np.ndarray, sw: np.ndarray, bf16: bool = False) -> np.ndarray:
+    """y = round((float(acc) * s_a) * s_w) (Cider README, "Quantization":
+    output dequant) to fp16, or with ``bf16`` to bf16 (returned as uint16 bit
+    patterns).  acc [M,N] or [M,N,1] -> [M,N]."""
     acc = _c(acc, np.int32)
     M, N = acc.shape[0], acc.shape[1]
     sa = _c(sa, np.float32)
     sw = _c(sw, np.float32)
     y = np.empty((M, N), np.uint16)
-    _load().oracle_dequant_pc(_ptr(acc), _ptr(sa), _ptr(sw), M, N, _ptr(y))
-    return y.view(np.float16)
+    fn = _load().oracle_dequant_pc_bf16 if bf16 else _load().oracle_dequant_pc
+    fn(_ptr(acc), _ptr(sa), _ptr(sw), M, N, _ptr(y))
+    return y if bf16 else y.view(np.float16)
 
 
-def dequant_pg(acc: np.ndarray, sa: np.ndarray, sw: np.ndarray) -> np.ndarray:
-    """y = fp16(sum_g in increasing g of (s_a * s_w[n,g]) * float(acc_g)).
-    acc [M,N,G], sw [N,G] -> fp16 [M,N]."""
+def dequant_pg(acc: np.ndarray, sa: np.ndarray, sw: np.ndarray, bf16: bool = False) -> np.ndarray:
+    """y = round(sum_g in increasing g of (s_a * s_w[n,g]) * float(acc_g)) to
+    fp16 (or bf16 bit patterns).  acc [M,N,G], sw [N,G] -> [M,N]."""
     acc = _c(acc, np.int32)
     M, N, G = acc.shape
     sa = _c(sa, np.float32)
     sw = _c(sw, np.float32)
     y = np.empty((M, N), np.uint16)
-    _load().oracle_dequant_pg(_ptr(acc), _ptr(sa), _ptr(sw), M, N, G, _ptr(y))
-    return y.view(np.float16)
+    fn = _load().oracle_dequant_pg_bf16 if bf16 else _load().oracle_dequant_pg
+    fn(_ptr(acc), _ptr(sa), _ptr(sw), M, N, G, _ptr(y))
+    return y if bf16 else y.view(np.float16)
 
 
 # ---------------------------------------------------------------- whole layer
 def linear(x_f16: np.ndarray, qw_values: np.ndarray, sw: np.ndarray,
-           group_size: int = 0, rows=None, threads: int = 1, bf16: bool = False) -> np.ndarray:
-    """The whole layer, y fp16 [len(rows), N], for the given activation rows
+           group_size: int = 0, rows=None, threads: int = 1, bf16: bool = False,
+           out_bf16: bool = False) -> np.ndarray:
+    """The whole layer, y [len(rows), N], for the given activation rows
     (default: all).  ``qw_values`` holds the integer weight values (INT8, or
     INT4 values from :func:`unpack_int4`).  With ``bf16`` the activations are
-    bf16 bit patterns (uint16 [M,K]).  Rows are independent, so ``threads > 1``
-    runs disjoint row ranges of the same single-threaded C code concurrently
-    (ctypes releases the GIL)."""
+    bf16 bit patterns (uint16 [M,K]); with ``out_bf16`` y is rounded to bf16
+    and returned as uint16 bit patterns (else fp16).  Rows are independent, so
+    ``threads > 1`` runs disjoint row ranges of the same single-threaded C
+    code concurrently (ctypes releases the GIL)."""
     x = _c(x_f16, np.uint16) if bf16 else f16_bits(x_f16)
     M, K = x.shape
     qw = _c(qw_values, np.int8)
@@ -248,11 +274,11 @@ def linear(x_f16: np.ndarray, qw_values: np.ndarray, sw: np.ndarray,
 
     def run(r0, r1):
         qa_s = np.empty((K,), np.int8)
-        acc_s = np.empty((N * G,), np.int32)
+        acc_s = np.empty((max(N * G, 1),), np.int32)
         r0, r1 = int(r0), int(r1)
-        fn = lib.oracle_linear_rows_bf16 if bf16 else lib.oracle_linear_rows
-        st = fn(_ptr(xs), K, N, _ptr(qw), _ptr(sw), group_size, r0, r1, _ptr(qa_s), _ptr(acc_s),
-                _ptr(y) + r0 * N * 2)
+        st = lib.oracle_linear_rows_ex(_ptr(xs), 1 if bf16 else 0, K, N, _ptr(qw), _ptr(sw),
+                                       group_size, r0, r1, _ptr(qa_s), _ptr(acc_s),
+                                       1 if out_bf16 else 0, _ptr(y) + r0 * N * 2)
         if st != 0:
             raise OverflowError("integer accumulator does not fit in int32")
 
@@ -262,7 +288,13 @@ def linear(x_f16: np.ndarray, qw_values: np.ndarray, sw: np.ndarray,
         bounds = np.linspace(0, R, min(threads, R) + 1).astype(int)
         with ThreadPoolExecutor(len(bounds) - 1) as ex:
             list(ex.map(lambda i: run(bounds[i], bounds[i + 1]), range(len(bounds) - 1)))
-    return y.view(np.float16)
+    return y if out_bf16 else y.view(np.float16)
+
+
+def f32_to_bf16(v: float) -> int:
+    """bf16 bit pattern of fp32 v, round to nearest even (the oracle's output
+    rounding for bf16 y)."""
+    return int(_load().oracle_f32_to_bf16(v))
 
 
 def f16_to_f32(bits: int) -> float:

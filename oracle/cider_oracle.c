@@ -34,6 +34,7 @@
 #include "cider_oracle.h"
 
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* ---- fp16 helpers (library conversions, no arithmetic of the method) ---- */
@@ -59,7 +60,21 @@ static float bf16_bits_to_f32(uint16_t bits) {
   return f;
 }
 
+/* fp32 -> bf16 bit pattern, round to nearest with ties to even on the 16
+ * bits dropped from the binary32 (so values past the bf16 range round to
+ * +-inf); NaN stays a quiet NaN.  Written from the definition of the bf16
+ * format: the upper half of a binary32. */
+static uint16_t f32_to_bf16_bits(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0u)
+    return (uint16_t)((u >> 16) | 0x0040u);
+  const uint32_t lsb = (u >> 16) & 1u;
+  return (uint16_t)((u + 0x7FFFu + lsb) >> 16);
+}
+
 float oracle_f16_to_f32(uint16_t bits) { return f16_bits_to_f32(bits); }
+uint16_t oracle_f32_to_bf16(float f) { return f32_to_bf16_bits(f); }
 uint16_t oracle_f32_to_f16(float f) { return f32_to_f16_bits(f); }
 
 /* ---- symmetric quantization of one block (shared by a1 and a2) ----
@@ -133,6 +148,59 @@ static void quantize_weight(const float* W, int64_t N, int64_t K,
   }
 }
 
+/* a2, percentile-clipped scales (Cider README "Notes": scales are min-max by
+ * default, or from a percentile with clip_percentile = 99.9).  Reading: the
+ * block's |W| values sorted ascending a_0 <= ... <= a_{n-1}; the p-th
+ * percentile with linear interpolation between closest ranks, at the
+ * fractional rank h = (n - 1) p / 100 (in double): lo = floor(h),
+ * hi = min(lo + 1, n - 1), t = (float)(h - lo) and
+ * clip = a_lo + t * (a_hi - a_lo) in fp32 (three roundings, no FMA).  The
+ * scale is clip / qdiv (1 when clip == 0) and codes clamp as for min-max, so
+ * values above clip saturate; p = 100 gives exactly the min-max result. */
+static int cmp_float(const void* a, const void* b) {
+  const float x = *(const float*)a, y = *(const float*)b;
+  return (x > y) - (x < y);
+}
+
+static float clipped_max(const float* blk, int64_t n, double p, float* tmp) {
+  for (int64_t j = 0; j < n; ++j) tmp[j] = fabsf(blk[j]);
+  qsort(tmp, (size_t)n, sizeof(float), cmp_float);
+  const double h = (double)(n - 1) * p / 100.0;
+  int64_t lo = (int64_t)floor(h);
+  if (lo > n - 1) lo = n - 1;
+  const int64_t hi = lo + 1 < n ? lo + 1 : n - 1;
+  const float t = (float)(h - (double)lo);
+  const float d = tmp[hi] - tmp[lo];
+  const float td = t * d;
+  return tmp[lo] + td;
+}
+
+static void quantize_weight_clip(const float* W, int64_t N, int64_t K, int64_t group_size,
+                                 double p, float qdiv, int qmin, int qmax, int8_t* q,
+                                 float* sw, float* tmp) {
+  int64_t gs = group_size > 0 ? group_size : K;
+  int64_t G = K / gs;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t g = 0; g < G; ++g) {
+      const float* blk = W + n * K + g * gs;
+      float s = block_scale(clipped_max(blk, gs, p, tmp), qdiv);
+      sw[n * G + g] = s;
+      for (int64_t j = 0; j < gs; ++j)
+        q[n * K + g * gs + j] = (int8_t)quantize_value(blk[j], s, qmin, qmax);
+    }
+}
+
+/* tmp: scratch of K floats */
+void oracle_quantize_weight_int8_clip(const float* W, int64_t N, int64_t K, int64_t group_size,
+                                      double clip_percentile, int8_t* qw, float* sw, float* tmp) {
+  quantize_weight_clip(W, N, K, group_size, clip_percentile, 127.0f, -127, 127, qw, sw, tmp);
+}
+
+void oracle_quantize_weight_int4_clip(const float* W, int64_t N, int64_t K, int64_t group_size,
+                                      double clip_percentile, int8_t* q4, float* sw, float* tmp) {
+  quantize_weight_clip(W, N, K, group_size, clip_percentile, 7.0f, -8, 7, q4, sw, tmp);
+}
+
 void oracle_quantize_weight_int8(const float* W, int64_t N, int64_t K,
                                  int64_t group_size, int8_t* qw, float* sw) {
   quantize_weight(W, N, K, group_size, 127.0f, -127, 127, qw, sw);
@@ -203,22 +271,24 @@ int oracle_gemm_acc(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N,
 }
 
 /* a5: per-channel dequant, C_fp16 = C_int32 * s_act * s_weight (Cider README
- * "Quantization" row "Output dequant"), evaluated left to right in fp32. */
-void oracle_dequant_pc(const int32_t* acc, const float* sa, const float* sw,
-                       int64_t M, int64_t N, uint16_t* y) {
+ * "Quantization" row "Output dequant"), evaluated left to right in fp32 and
+ * rounded once to the output format (fp16, or bf16: the README roadmap's
+ * "auto dtype float16/bfloat16"). */
+static void dequant_pc(const int32_t* acc, const float* sa, const float* sw, int64_t M, int64_t N,
+                       uint16_t (*narrow)(float), uint16_t* y) {
   for (int64_t m = 0; m < M; ++m)
     for (int64_t n = 0; n < N; ++n) {
       float v = (float)acc[m * N + n];
       v = v * sa[m];
       v = v * sw[n];
-      y[m * N + n] = f32_to_f16_bits(v);
+      y[m * N + n] = narrow(v);
     }
 }
 
 /* a5: per-group dequant: fp32 sum over groups in increasing g of
- * (s_a * s_w[n,g]) * acc_g, then one rounding to fp16. */
-void oracle_dequant_pg(const int32_t* acc, const float* sa, const float* sw,
-                       int64_t M, int64_t N, int64_t G, uint16_t* y) {
+ * (s_a * s_w[n,g]) * acc_g, then one rounding to the output format. */
+static void dequant_pg(const int32_t* acc, const float* sa, const float* sw, int64_t M, int64_t N,
+                       int64_t G, uint16_t (*narrow)(float), uint16_t* y) {
   for (int64_t m = 0; m < M; ++m)
     for (int64_t n = 0; n < N; ++n) {
       float s = 0.0f;
@@ -227,19 +297,39 @@ void oracle_dequant_pg(const int32_t* acc, const float* sa, const float* sw,
         float term = scale * (float)acc[(m * N + n) * G + g];
         s = s + term;
       }
-      y[m * N + n] = f32_to_f16_bits(s);
+      y[m * N + n] = narrow(s);
     }
+}
+
+void oracle_dequant_pc(const int32_t* acc, const float* sa, const float* sw,
+                       int64_t M, int64_t N, uint16_t* y) {
+  dequant_pc(acc, sa, sw, M, N, f32_to_f16_bits, y);
+}
+
+void oracle_dequant_pg(const int32_t* acc, const float* sa, const float* sw,
+                       int64_t M, int64_t N, int64_t G, uint16_t* y) {
+  dequant_pg(acc, sa, sw, M, N, G, f32_to_f16_bits, y);
+}
+
+void oracle_dequant_pc_bf16(const int32_t* acc, const float* sa, const float* sw,
+                            int64_t M, int64_t N, uint16_t* y) {
+  dequant_pc(acc, sa, sw, M, N, f32_to_bf16_bits, y);
+}
+
+void oracle_dequant_pg_bf16(const int32_t* acc, const float* sa, const float* sw,
+                            int64_t M, int64_t N, int64_t G, uint16_t* y) {
+  dequant_pg(acc, sa, sw, M, N, G, f32_to_bf16_bits, y);
 }
 
 /* The whole layer for activation rows [m0, m1): quantize those rows, form the
  * integer accumulators, dequantize.  qw holds unpacked weight values (INT8, or
  * INT4 values after oracle_unpack_int4).  group_size = 0 -> per-channel.
- * y receives (m1 - m0) rows of N fp16 values.  acc_scratch must hold
- * N * G int32; qa_scratch K int8.  Returns the GEMM status. */
+ * y receives (m1 - m0) rows of N fp16 (or bf16) values.  acc_scratch must
+ * hold N * G int32; qa_scratch K int8.  Returns the GEMM status. */
 static int linear_rows(const uint16_t* x, float (*widen)(uint16_t), int64_t K, int64_t N,
                        const int8_t* qw, const float* sw, int64_t group_size,
                        int64_t m0, int64_t m1, int8_t* qa_scratch,
-                       int32_t* acc_scratch, uint16_t* y) {
+                       int32_t* acc_scratch, uint16_t (*narrow)(float), uint16_t* y) {
   int64_t G = group_size > 0 ? K / group_size : 1;
   int status = 0;
   for (int64_t m = m0; m < m1; ++m) {
@@ -249,9 +339,9 @@ static int linear_rows(const uint16_t* x, float (*widen)(uint16_t), int64_t K, i
       status = -1;
     uint16_t* yrow = y + (m - m0) * N;
     if (group_size > 0)
-      oracle_dequant_pg(acc_scratch, &sa, sw, 1, N, G, yrow);
+      dequant_pg(acc_scratch, &sa, sw, 1, N, G, narrow, yrow);
     else
-      oracle_dequant_pc(acc_scratch, &sa, sw, 1, N, yrow);
+      dequant_pc(acc_scratch, &sa, sw, 1, N, narrow, yrow);
   }
   return status;
 }
@@ -261,7 +351,7 @@ int oracle_linear_rows(const uint16_t* x_f16, int64_t K, int64_t N,
                        int64_t m0, int64_t m1, int8_t* qa_scratch,
                        int32_t* acc_scratch, uint16_t* y) {
   return linear_rows(x_f16, f16_bits_to_f32, K, N, qw, sw, group_size, m0, m1, qa_scratch,
-                     acc_scratch, y);
+                     acc_scratch, f32_to_f16_bits, y);
 }
 
 int oracle_linear_rows_bf16(const uint16_t* x_bf16, int64_t K, int64_t N,
@@ -269,5 +359,14 @@ int oracle_linear_rows_bf16(const uint16_t* x_bf16, int64_t K, int64_t N,
                             int64_t m0, int64_t m1, int8_t* qa_scratch,
                             int32_t* acc_scratch, uint16_t* y) {
   return linear_rows(x_bf16, bf16_bits_to_f32, K, N, qw, sw, group_size, m0, m1, qa_scratch,
-                     acc_scratch, y);
+                     acc_scratch, f32_to_f16_bits, y);
+}
+
+int oracle_linear_rows_ex(const uint16_t* x, int x_bf16, int64_t K, int64_t N,
+                          const int8_t* qw, const float* sw, int64_t group_size,
+                          int64_t m0, int64_t m1, int8_t* qa_scratch,
+                          int32_t* acc_scratch, int y_bf16, uint16_t* y) {
+  return linear_rows(x, x_bf16 ? bf16_bits_to_f32 : f16_bits_to_f32, K, N, qw, sw, group_size,
+                     m0, m1, qa_scratch, acc_scratch, y_bf16 ? f32_to_bf16_bits : f32_to_f16_bits,
+                     y);
 }

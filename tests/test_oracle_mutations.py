@@ -40,6 +40,12 @@ MUTATIONS = [
      "quantize_act_rows(x_bf16, M, K, f16_bits_to_f32, qa, sa);"),
     ("offset_zero_point_7", "int lo = (int)(src[i] & 0xFu) - 8;", "int lo = (int)(src[i] & 0xFu) - 7;"),
     ("offset_high_nibble_kept", "int hi = (int)(src[i] >> 4) - 8;", "int hi = nibble_value(src[i] >> 4);"),
+    ("bf16_truncate", "return (uint16_t)((u + 0x7FFFu + lsb) >> 16);", "return (uint16_t)(u >> 16);"),
+    ("bf16_ties_away", "return (uint16_t)((u + 0x7FFFu + lsb) >> 16);",
+     "return (uint16_t)((u + 0x8000u) >> 16);"),
+    ("clip_rank_n", "const double h = (double)(n - 1) * p / 100.0;",
+     "const double h = (double)n * p / 100.0;"),
+    ("clip_nearest_lower_rank", "const float t = (float)(h - (double)lo);", "const float t = 0.0f;"),
 ]
 
 PIN_TESTS = [
@@ -65,6 +71,11 @@ PIN_TESTS = [
     pins.test_quantize_act_bf16_agrees_with_fp16_on_shared_values,
     pins.test_int4_offset_binary_hand_worked,
     pins.test_int4_offset_binary_exhaustive,
+    pins.test_bf16_output_rounding_matches_pytorch,
+    pins.test_dequant_bf16_special_cases,
+    pins.test_clip_percentile_hand_worked_cases,
+    lambda: pins.test_clip_percentile_matches_numpy_linear_percentile(128, 99.9),
+    lambda: pins.test_clip_percentile_100_is_min_max(64),
 ]
 
 

@@ -443,3 +443,131 @@ def test_int4_offset_binary_exhaustive():
     vals = oracle.unpack_int4(dst[None, :])[0].astype(np.int16)
     np.testing.assert_array_equal(vals[0::2], (src & 0xF).astype(np.int16) - 8)
     np.testing.assert_array_equal(vals[1::2], (src >> 4).astype(np.int16) - 8)
+
+
+# ---------------------------------------------------------------- bf16 outputs
+def _torch_bf16_bits(v: np.ndarray) -> np.ndarray:
+    """PyTorch's fp32 -> bf16 conversion (round to nearest even), as uint16."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(torch.bfloat16).view(
+        torch.int16).numpy().view(np.uint16)
+
+
+def test_bf16_output_rounding_matches_pytorch():
+    """The oracle's fp32 -> bf16 rounding against PyTorch's conversion: every
+    tie pattern around 1.0 and 2^-126, values past the bf16 range, bf16 and
+    fp32 subnormals, signs, and random values."""
+    ties = []
+    for base in (0x3F800000, 0x3F810000, 0x00800000, 0x7F7F0000, 0x00010000):
+        for low in (0x0000, 0x0001, 0x7FFF, 0x8000, 0x8001, 0xFFFF):
+            ties.append(base | low)
+    rng = np.random.default_rng(5)
+    bits = np.concatenate([np.array(ties, np.uint32), rng.integers(0, 0x7F800000, 20000, dtype=np.uint32)])
+    bits = np.concatenate([bits, bits | 0x80000000])
+    vals = bits.view(np.float32)
+    got = np.array([oracle.f32_to_bf16(float(v)) for v in vals], np.uint16)
+    assert np.array_equal(got, _torch_bf16_bits(vals))
+    # one hand case per rule: 1 + 2^-8 is halfway between 1 and 1 + 2^-7 (even: 1),
+    # 1 + 3 * 2^-8 halfway between 1 + 2^-7 and 1 + 2^-6 (even: the latter); the
+    # largest fp32 rounds past the bf16 range to +inf
+    assert oracle.f32_to_bf16(1.00390625) == 0x3F80
+    assert oracle.f32_to_bf16(1.01171875) == 0x3F82
+    assert oracle.f32_to_bf16(float(np.finfo(np.float32).max)) == 0x7F80
+
+
+def test_dequant_bf16_special_cases():
+    """s_a = s_w = 1 and |acc| <= 256: y is acc exactly (integers up to 2^8
+    are bf16 values); per group with one group equals per channel; doubling
+    every s_w doubles y; and where the fp32 result is exact in both formats
+    (small integers) the bf16 and fp16 outputs hold the same value."""
+    acc = np.arange(-256, 257, dtype=np.int32).reshape(1, -1)
+    ones_a = np.ones(1, np.float32)
+    ones_w = np.ones(acc.shape[1], np.float32)
+    y = oracle.dequant_pc(acc, ones_a, ones_w, bf16=True)
+    assert np.array_equal(y, _torch_bf16_bits(acc.astype(np.float32)))
+    assert np.array_equal((y.astype(np.uint32) << 16).view(np.float32), acc.astype(np.float32))
+    yh = oracle.dequant_pc(acc, ones_a, ones_w)
+    assert np.array_equal((y.astype(np.uint32) << 16).view(np.float32), yh.astype(np.float32))
+    rng = np.random.default_rng(6)
+    acc = rng.integers(-2 ** 20, 2 ** 20, (4, 40)).astype(np.int32)
+    sa = (rng.random(4) * 1e-2 + 1e-3).astype(np.float32)
+    sw = (rng.random(40) * 1e-3 + 1e-4).astype(np.float32)
+    ypc = oracle.dequant_pc(acc, sa, sw, bf16=True)
+    assert np.array_equal(oracle.dequant_pg(acc[:, :, None], sa, sw[:, None], bf16=True), ypc)
+    y2 = oracle.dequant_pc(acc, sa, 2 * sw, bf16=True)
+    assert np.array_equal((y2.astype(np.uint32) << 16).view(np.float32),
+                          2 * (ypc.astype(np.uint32) << 16).view(np.float32))
+
+
+def test_linear_bf16_output_is_the_fp16_paths_fp32_value_rounded_otherwise():
+    """The whole layer with bf16 y and with fp16 y differ only in the last
+    rounding: both are within half an ulp (of their own format) of one fp32
+    value, so the two outputs lie within half a bf16 ulp plus half an fp16 ulp
+    of each other, and they agree exactly wherever that fp32 value is exact in
+    both formats (checked via all-zero rows)."""
+    from w4a8_quantized_linear_gb300 import inputs
+    x = inputs.activations(6, 256, seed=3)
+    x[2] = 0
+    W = inputs.weights(40, 256, seed=4)
+    for gs in (0, 64):
+        qw, sw = oracle.quantize_weight_int8(W, gs)
+        yb = oracle.linear(x, qw, sw, gs, out_bf16=True)
+        yh = oracle.linear(x, qw, sw, gs)
+        fb = (yb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        fh = yh.astype(np.float64)
+        ulp_b = np.spacing(np.abs(fb).astype(np.float32)).astype(np.float64) * 2.0 ** 16
+        ulp_h = np.spacing(np.abs(yh)).astype(np.float64)
+        assert np.all(np.abs(fb - fh) <= 0.5 * ulp_b + 0.5 * ulp_h)
+        assert np.all(fb[2] == 0) and np.all(fh[2] == 0)
+
+
+# ---------------------------------------------------------------- clipped scales
+def _read_clip_golden():
+    here = os.path.dirname(os.path.abspath(__file__))
+    blocks = {"arange1_100": np.arange(1, 101, dtype=np.float32),
+              "m3_1_2_4": np.array([-3, 1, 2, 4], np.float32),
+              "z0_0_0_5": np.array([0, 0, 0, 5], np.float32)}
+    rows = []
+    with open(os.path.join(here, "golden", "clip_percentile_hand.txt")) as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            name, p, qmax, s_hex, codes = [t.strip() for t in line.split("|")]
+            rows.append((blocks[name], float(p), int(qmax), int(s_hex, 16),
+                         np.array(codes.split(), np.int64)))
+    return rows
+
+
+def test_clip_percentile_hand_worked_cases():
+    for blk, p, qmax, s_bits, codes in _read_clip_golden():
+        W = blk.reshape(1, -1)
+        if qmax == 127:
+            q, s = oracle.quantize_weight_int8(W, 0, clip_percentile=p)
+        else:
+            q, s = oracle.quantize_weight_int4(W, 0, clip_percentile=p)
+        assert int(s.view(np.uint32)[0, 0]) == s_bits, (blk, p, hex(int(s.view(np.uint32)[0, 0])))
+        assert np.array_equal(q[0, -len(codes):].astype(np.int64), codes), (blk, p, q)
+
+
+@pytest.mark.parametrize("gs", [0, 64, 128])
+def test_clip_percentile_100_is_min_max(gs):
+    from w4a8_quantized_linear_gb300 import inputs
+    W = inputs.weights(24, 512, seed=9)
+    W[3] = 0
+    for f in (oracle.quantize_weight_int8, oracle.quantize_weight_int4):
+        q1, s1 = f(W, gs, clip_percentile=100.0)
+        q0, s0 = f(W, gs)
+        assert np.array_equal(q1, q0) and np.array_equal(s1.view(np.uint32), s0.view(np.uint32))
+
+
+@pytest.mark.parametrize("n", [4, 64, 128, 2560])
+@pytest.mark.parametrize("p", [99.9, 99.0, 95.0, 50.0, 0.1])
+def test_clip_percentile_matches_numpy_linear_percentile(n, p):
+    """The clip value behind each scale against numpy.percentile (linear
+    interpolation between closest ranks, computed in float64): equal to a few
+    fp32 roundings (the oracle's interpolation is in fp32)."""
+    rng = np.random.default_rng(n + int(p * 10))
+    W = (rng.standard_normal((8, n)) * 0.02).astype(np.float32)
+    q, s = oracle.quantize_weight_int8(W, 0, clip_percentile=p)
+    want = np.percentile(np.abs(W).astype(np.float64), p, axis=1, method="linear") / 127.0
+    assert np.allclose(s[:, 0].astype(np.float64), want, rtol=4e-7, atol=0)
