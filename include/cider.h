@@ -64,6 +64,11 @@ typedef enum {
 
 typedef enum { CIDER_PER_CHANNEL = 0, CIDER_PER_GROUP = 1 } cider_granularity_t;
 
+/* Element type of an activation or output matrix (the Cider README's roadmap,
+ * "auto dtype float16/bfloat16"): IEEE binary16, or bfloat16 (the upper half
+ * of an IEEE binary32). */
+typedef enum { CIDER_F16 = 0, CIDER_BF16 = 1 } cider_dtype_t;
+
 /* 1 when the current CUDA device is an sm_103 GPU this library was built
  * for, else 0 (the Cider README's is_available(), "Conditional compilation").
  * The environment variable CIDER_FORCE_UNSUPPORTED=1 forces 0. */
@@ -110,6 +115,26 @@ cider_status_t cider_quantize_weight_int8(const float* w, int64_t N, int64_t K,
 cider_status_t cider_quantize_weight_int4(const float* w, int64_t N, int64_t K,
                                           int group_size, uint8_t* qw_packed,
                                           float* sw, void* stream);
+
+/* The two weight quantizers with percentile-clipped scales (Cider README,
+ * "Notes": scales are min-max by default, or a percentile method,
+ * clip_percentile=99.9).  Per block (a row for group_size 0, else each
+ * group_size-element block) of n values: the |W| values sorted ascending
+ * a_0 <= ... <= a_{n-1}; the fractional rank h = (n - 1) * clip_percentile /
+ * 100 (in double), lo = floor(h), hi = min(lo + 1, n - 1),
+ * t = (float)(h - lo); clip = a_lo + t * (a_hi - a_lo) in fp32 (no FMA);
+ * s_w = clip / 127 (INT8) or clip / 7 (INT4), 1 when clip is 0; codes as in
+ * the min-max quantizers, so values above the clip saturate at the code range.
+ * clip_percentile = 100 gives exactly the min-max result.
+ *   clip_percentile  in (0, 100]; anything else (or NaN) gives
+ *                    CIDER_ERR_INVALID_ARGUMENT before any other check.
+ *   Other arguments, layouts and checks as cider_quantize_weight_int8 / _int4. */
+cider_status_t cider_quantize_weight_int8_clip(const float* w, int64_t N, int64_t K,
+                                               int group_size, double clip_percentile,
+                                               int8_t* qw, float* sw, void* stream);
+cider_status_t cider_quantize_weight_int4_clip(const float* w, int64_t N, int64_t K,
+                                               int group_size, double clip_percentile,
+                                               uint8_t* qw_packed, float* sw, void* stream);
 
 /* W8A8 linear: y = dequant(quant(x) x qw^T) (Cider README, "Low-level API":
  * perchannel_linear; "Metal kernel pipeline": quantize_per_token then
@@ -189,6 +214,24 @@ cider_status_t cider_w4a8_accumulators(const int8_t* qa, int64_t M, int64_t N,
                                        int64_t K, const uint8_t* qw_packed,
                                        int group_size, int32_t* acc,
                                        void* stream);
+
+/* The linears with the activation and output element types chosen per call
+ * (Cider README, "Roadmap": "auto dtype float16/bfloat16").
+ *   x       [M, K] of x_dtype (CIDER_F16 or CIDER_BF16); a bf16 value widens
+ *           exactly to fp32, then the steps are those of cider_w8a8_linear.
+ *   y       [M, N] of y_dtype: the same fp32 result as for fp16 output (per
+ *           channel (acc * s_a) * s_w; per group the sum over g of
+ *           (s_a * s_w[n,g]) * acc_g), rounded once to y_dtype, round to
+ *           nearest even (so bf16 y is not fp16 y converted).
+ *   Other arguments, checks and errors as cider_w8a8_linear / cider_w4a8_linear;
+ *   an x_dtype or y_dtype outside the enum gives CIDER_ERR_INVALID_ARGUMENT.
+ *   (dtypes F16/F16 is cider_w8a8_linear, BF16/F16 cider_w8a8_linear_bf16.) */
+cider_status_t cider_w8a8_linear_ex(const void* x, int x_dtype, int64_t M, int64_t N, int64_t K,
+                                    const int8_t* qw, const float* sw, int granularity,
+                                    int group_size, void* y, int y_dtype, void* stream);
+cider_status_t cider_w4a8_linear_ex(const void* x, int x_dtype, int64_t M, int64_t N, int64_t K,
+                                    const uint8_t* qw_packed, const float* sw, int granularity,
+                                    int group_size, void* y, int y_dtype, void* stream);
 
 /* Size of the fixed scratch array used by cider_w8a8_linear_noalloc: 32 MiB
  * of device global memory per GPU on which the library has been used. */

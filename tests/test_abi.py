@@ -167,3 +167,27 @@ def test_debug_split_queries_need_no_device(lib):
     assert lib.cider_debug_small_m_slices(16, 2560, 10240, 0, 0, 152, ctypes.byref(ks)) == OK
     assert ks.value > 1
     assert lib.cider_debug_small_m_slices(0, 2560, 10240, 0, 0, 152, ctypes.byref(ks)) == INVALID
+
+
+def test_dtype_linears_and_clipped_quantizers_check_arguments(lib, no_device):
+    """The dtype-aware linears and the percentile-clipped weight quantizers:
+    bad dtypes and percentiles are rejected, well-formed calls stop at the
+    device check (no GPU involved)."""
+    for fn in ("cider_w8a8_linear_ex", "cider_w4a8_linear_ex"):
+        f = getattr(lib, fn)
+        assert f(P, 0, 4, 64, 256, P, P, 0, 0, P, 1, None) == UNSUPPORTED
+        assert f(P, 1, 4, 64, 256, P, P, 1, 128, P, 0, None) == UNSUPPORTED
+        assert f(P, 2, 4, 64, 256, P, P, 0, 0, P, 0, None) == INVALID      # unknown x dtype
+        assert f(P, 0, 4, 64, 256, P, P, 0, 0, P, -1, None) == INVALID     # unknown y dtype
+        assert f(None, 0, 4, 64, 256, P, P, 0, 0, P, 1, None) == INVALID
+        assert f(P, 0, 4, 64, 100, P, P, 0, 0, P, 1, None) == INVALID      # K % 32
+        assert f(P + 8, 0, 4, 64, 256, P, P, 0, 0, P, 1, None) == MISALIGNED
+        assert f(P, 0, 0, 64, 256, P, P, 0, 0, P, 1, None) == 0              # empty problem
+    for fn in ("cider_quantize_weight_int8_clip", "cider_quantize_weight_int4_clip"):
+        f = getattr(lib, fn)
+        assert f(P, 8, 256, 64, 99.9, P, P, None) == UNSUPPORTED
+        assert f(P, 8, 256, 0, 100.0, P, P, None) == UNSUPPORTED
+        for bad in (0.0, -1.0, 100.5, float("nan")):
+            assert f(P, 8, 256, 64, bad, P, P, None) == INVALID
+        assert f(P, 8, 256, 96, 99.9, P, P, None) == INVALID                 # group size
+        assert f(P + 1, 8, 256, 0, 99.9, P, P, None) == MISALIGNED

@@ -117,3 +117,60 @@ def test_offset_binary_weights_give_the_same_linear(cider):
 
 def test_no_device_error_left(cider):
     assert cider.cider_check_device_error() == 0
+
+
+# ---------------------------------------------------------------- bf16 outputs
+def _bf16_as_f64(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def assert_bf16_close(y_bits, ref_bits, what=""):
+    """|y - y_ref| <= 2e-3 max|y_ref| + 1 bf16 ulp(y_ref): the output
+    tolerance, with the ulp of the output's own format."""
+    y, r = _bf16_as_f64(y_bits), _bf16_as_f64(ref_bits)
+    assert np.all(np.isfinite(r))
+    ulp = np.spacing(np.abs(r).astype(np.float32)).astype(np.float64) * 2.0 ** 16
+    bound = 2e-3 * np.max(np.abs(r)) + ulp
+    bad = np.abs(y - r) > bound
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} out of tolerance"
+
+
+@pytest.mark.parametrize("x_bf16", [False, True])
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("gs", [0, 128, 64])
+@pytest.mark.parametrize("M,N,K", [(1, 264, 1024), (3, 136, 2560), (16, 520, 4096), (2, 264, 8192),
+                                   (200, 264, 1024), (300, 520, 2048)])
+def test_linear_bf16_output_matches_oracle(cider, M, N, K, gs, bits, x_bf16):
+    """y in bf16 through the small-M path (with and without K slices) and the
+    two tensor-core GEMMs: per channel bit for bit, per group within the
+    tolerance, against the oracle's single rounding of the same fp32 value."""
+    if bits == 4 and gs == 64:
+        pytest.skip("covered by the 8-bit case")
+    if x_bf16:
+        xb = inputs.activations_bf16(M, K, seed=600 + M)
+        xd = bf16_dev(xb)
+        x_or = xb
+    else:
+        x_or = inputs.activations(M, K, seed=600 + M)
+        xd = to_dev(x_or)
+    W = inputs.weights(N, K, seed=601)
+    if bits == 8:
+        qw, sw = oracle.quantize_weight_int8(W, gs)
+        qv, fn = qw, cider.cider_w8a8_linear_ex
+    else:
+        q4, sw = oracle.quantize_weight_int4(W, gs)
+        qw, qv, fn = oracle.pack_int4(q4), q4, cider.cider_w4a8_linear_ex
+    y = fn(xd, to_dev(qw), to_dev(sw), gs, y_dtype=torch.bfloat16)
+    assert y.dtype == torch.bfloat16
+    yb = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = oracle.linear(x_or, qv, sw, gs, threads=8, bf16=x_bf16, out_bf16=True)
+    what = f"bf16 y M={M} N={N} K={K} gs={gs} bits={bits} x_bf16={x_bf16}"
+    if gs == 0:
+        assert_bits_equal(yb, ref, what)
+    else:
+        assert_bf16_close(yb, ref, what)
+    # fp16 output through the same entry point is the fp16 linear, bit for bit
+    yh = fn(xd, to_dev(qw), to_dev(sw), gs, y_dtype=torch.float16)
+    base = (cider.cider_w8a8_linear_bf16 if bits == 8 else cider.cider_w4a8_linear_bf16) if x_bf16 \
+        else (cider.cider_w8a8_linear if bits == 8 else cider.cider_w4a8_linear)
+    assert_bits_equal(to_host(yh), to_host(base(xd, to_dev(qw), to_dev(sw), gs)), what + " (fp16)")

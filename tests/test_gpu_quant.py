@@ -149,3 +149,28 @@ def test_fused_gemv_quantization_sampled_fp16_values(cider, M):
         acc = qref[r0:r0 + M].astype(np.int32)
         want = oracle.dequant_pc(acc, sref[r0:r0 + M], sw)
         assert_bits_equal(y, want, f"fused GEMV M={M}, rows {r0}..{r0 + M - 1}, amax {amax}")
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("gs", [0, 64, 128])
+@pytest.mark.parametrize("p", [99.9, 99.0, 50.0, 100.0, 0.1])
+@pytest.mark.parametrize("N,K", [(16, 128), (40, 2560), (8, 12288)])
+def test_quantize_weight_clip_bit_exact(cider, N, K, gs, p, bits):
+    """Percentile-clipped weight scales and codes (the radix select of whole
+    rows, the rank count of 64 / 128-element groups) bit for bit against the
+    oracle, with ties, zero blocks and outliers planted."""
+    W = inputs.weights(N, K, seed=int(p * 10) + K)
+    W[1] = 0.0                                   # an all-zero row
+    W[2, :64] = 0.0                              # an all-zero first group
+    W[3, ::7] = 0.25                             # many equal values (ties)
+    W[4, 5] = 3.0                                # one outlier above the clip
+    W[5] = np.float32(0.0125)                    # a constant row
+    fn = cider.cider_quantize_weight_int8 if bits == 8 else cider.cider_quantize_weight_int4
+    qd, sd = fn(to_dev(W), gs, clip_percentile=p)
+    if bits == 8:
+        qref, sref = oracle.quantize_weight_int8(W, gs, clip_percentile=p)
+    else:
+        q4, sref = oracle.quantize_weight_int4(W, gs, clip_percentile=p)
+        qref = oracle.pack_int4(q4)
+    assert_bits_equal(to_host(sd).view(np.uint32), sref.view(np.uint32), f"clip s_w p={p} gs={gs}")
+    assert_bits_equal(to_host(qd), qref, f"clip q_w p={p} gs={gs}")

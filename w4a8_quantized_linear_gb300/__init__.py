@@ -25,6 +25,9 @@ HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "cider.h")
 CIDER_OK = 0
 CIDER_PER_CHANNEL = 0
 CIDER_PER_GROUP = 1
+CIDER_F16 = 0
+CIDER_BF16 = 1
+_DTYPES = {torch.float16: CIDER_F16, torch.bfloat16: CIDER_BF16}
 STATUS_NAMES = {0: "CIDER_OK", 1: "CIDER_ERR_INVALID_ARGUMENT", 2: "CIDER_ERR_MISALIGNED",
                 3: "CIDER_ERR_UNSUPPORTED_DEVICE", 4: "CIDER_ERR_CUDA", 5: "CIDER_ERR_TIMEOUT"}
 
@@ -50,10 +53,14 @@ def _declare(lib):
         "cider_int4_from_offset_binary": ([p, p, i64, p], i32),
         "cider_quantize_weight_int8": ([p, i64, i64, i32, p, p, p], i32),
         "cider_quantize_weight_int4": ([p, i64, i64, i32, p, p, p], i32),
+        "cider_quantize_weight_int8_clip": ([p, i64, i64, i32, ctypes.c_double, p, p, p], i32),
+        "cider_quantize_weight_int4_clip": ([p, i64, i64, i32, ctypes.c_double, p, p, p], i32),
         "cider_w8a8_linear": ([p, i64, i64, i64, p, p, i32, i32, p, p], i32),
         "cider_w4a8_linear": ([p, i64, i64, i64, p, p, i32, i32, p, p], i32),
         "cider_w8a8_linear_bf16": ([p, i64, i64, i64, p, p, i32, i32, p, p], i32),
         "cider_w4a8_linear_bf16": ([p, i64, i64, i64, p, p, i32, i32, p, p], i32),
+        "cider_w8a8_linear_ex": ([p, i32, i64, i64, i64, p, p, i32, i32, p, i32, p], i32),
+        "cider_w4a8_linear_ex": ([p, i32, i64, i64, i64, p, p, i32, i32, p, i32, p], i32),
         "cider_w8a8_linear_prequant": ([p, p, i64, i64, i64, p, p, i32, i32, p, p], i32),
         "cider_w4a8_linear_prequant": ([p, p, i64, i64, i64, p, p, i32, i32, p, p], i32),
         "cider_w8a8_accumulators": ([p, i64, i64, i64, p, i32, p, p], i32),
@@ -153,29 +160,43 @@ def cider_int4_from_offset_binary(packed: torch.Tensor, out=None):
     return dst
 
 
-def cider_quantize_weight_int8(w: torch.Tensor, group_size: int = 0):
-    """w fp32 [N, K] -> (qw int8 [N, K], sw fp32 [N, G])."""
+def cider_quantize_weight_int8(w: torch.Tensor, group_size: int = 0, clip_percentile=None):
+    """w fp32 [N, K] -> (qw int8 [N, K], sw fp32 [N, G]); min-max scales, or
+    percentile-clipped ones when ``clip_percentile`` (in (0, 100]) is given."""
     _need(w, torch.float32, "w", 2)
     N, K = w.shape
     G = K // group_size if group_size else 1
     qw = torch.empty((N, K), dtype=torch.int8, device=w.device)
     sw = torch.empty((N, G), dtype=torch.float32, device=w.device)
-    _check("cider_quantize_weight_int8",
-           _load().cider_quantize_weight_int8(_ptr(w), N, K, group_size, _ptr(qw), _ptr(sw),
-                                              _stream(w)))
+    if clip_percentile is None:
+        _check("cider_quantize_weight_int8",
+               _load().cider_quantize_weight_int8(_ptr(w), N, K, group_size, _ptr(qw), _ptr(sw),
+                                                  _stream(w)))
+    else:
+        _check("cider_quantize_weight_int8_clip",
+               _load().cider_quantize_weight_int8_clip(_ptr(w), N, K, group_size,
+                                                       float(clip_percentile), _ptr(qw), _ptr(sw),
+                                                       _stream(w)))
     return qw, sw
 
 
-def cider_quantize_weight_int4(w: torch.Tensor, group_size: int = 0):
-    """w fp32 [N, K] -> (packed uint8 [N, K/2], sw fp32 [N, G])."""
+def cider_quantize_weight_int4(w: torch.Tensor, group_size: int = 0, clip_percentile=None):
+    """w fp32 [N, K] -> (packed uint8 [N, K/2], sw fp32 [N, G]); min-max or
+    percentile-clipped scales as for the INT8 quantizer."""
     _need(w, torch.float32, "w", 2)
     N, K = w.shape
     G = K // group_size if group_size else 1
     qp = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
     sw = torch.empty((N, G), dtype=torch.float32, device=w.device)
-    _check("cider_quantize_weight_int4",
-           _load().cider_quantize_weight_int4(_ptr(w), N, K, group_size, _ptr(qp), _ptr(sw),
-                                              _stream(w)))
+    if clip_percentile is None:
+        _check("cider_quantize_weight_int4",
+               _load().cider_quantize_weight_int4(_ptr(w), N, K, group_size, _ptr(qp), _ptr(sw),
+                                                  _stream(w)))
+    else:
+        _check("cider_quantize_weight_int4_clip",
+               _load().cider_quantize_weight_int4_clip(_ptr(w), N, K, group_size,
+                                                       float(clip_percentile), _ptr(qp), _ptr(sw),
+                                                       _stream(w)))
     return qp, sw
 
 
@@ -218,6 +239,36 @@ def cider_w4a8_linear_bf16(x, qw_packed, sw, group_size: int = 0, out=None):
     """As cider_w4a8_linear for x bf16 [M, K]; y is fp16."""
     return _linear("cider_w4a8_linear_bf16", x, qw_packed, sw, group_size, True, out,
                    torch.bfloat16)
+
+
+def _linear_ex(fn, x, qw, sw, group_size, int4, y_dtype, out):
+    if x.dtype not in _DTYPES or y_dtype not in _DTYPES:
+        raise TypeError("x and y must be float16 or bfloat16")
+    _need(x, x.dtype, "x", 2)
+    _need(qw, torch.uint8 if int4 else torch.int8, "qw", 2)
+    M, K = x.shape
+    N = qw.shape[0]
+    if qw.shape[1] != (K // 2 if int4 else K):
+        raise ValueError("weight width does not match K")
+    sw = sw.reshape(N, -1)
+    _need(sw, torch.float32, "sw", 2)
+    y = out if out is not None else torch.empty((M, N), dtype=y_dtype, device=x.device)
+    _need(y, y_dtype, "out", 2)
+    _check(fn, getattr(_load(), fn)(_ptr(x), _DTYPES[x.dtype], M, N, K, _ptr(qw), _ptr(sw),
+                                    _gran(group_size), group_size, _ptr(y), _DTYPES[y_dtype],
+                                    _stream(x)))
+    return y
+
+
+def cider_w8a8_linear_ex(x, qw, sw, group_size: int = 0, y_dtype=torch.float16, out=None):
+    """W8A8 linear with x fp16 or bf16 [M, K] and y of ``y_dtype`` (fp16 or
+    bf16, the fp32 result rounded once to it)."""
+    return _linear_ex("cider_w8a8_linear_ex", x, qw, sw, group_size, False, y_dtype, out)
+
+
+def cider_w4a8_linear_ex(x, qw_packed, sw, group_size: int = 0, y_dtype=torch.float16, out=None):
+    """W4A8 linear with x fp16 or bf16 [M, K] and y of ``y_dtype``."""
+    return _linear_ex("cider_w4a8_linear_ex", x, qw_packed, sw, group_size, True, y_dtype, out)
 
 
 def _linear_prequant(fn, qa, sa, qw, sw, group_size, int4, out=None):

@@ -134,8 +134,9 @@ cider_status_t guarded(F&& f) {
   }
 }
 
+// clip_percentile < 0: min-max scales; else percentile-clipped ones.
 cider_status_t quantize_weight(const float* w, int64_t N, int64_t K, int group_size, void* q,
-                               float* sw, bool int4, void* stream) {
+                               float* sw, bool int4, void* stream, double clip_percentile = -1.0) {
   if (N == 0) return CIDER_OK;
   if (N < 0 || N > kMaxDim || !w || !q || !sw || !valid_k(K)) return CIDER_ERR_INVALID_ARGUMENT;
   if (!(group_size == 0 || ((group_size == 64 || group_size == 128) && K % group_size == 0)))
@@ -144,10 +145,16 @@ cider_status_t quantize_weight(const float* w, int64_t N, int64_t K, int group_s
   if (!aligned(sw, 4)) return CIDER_ERR_MISALIGNED;
   cider_status_t s = cider::check_device(nullptr, nullptr);
   if (s != CIDER_OK) return s;
+  if (clip_percentile >= 0.0)
+    return cuda_status(cider::launch_quant_weight_clip(w, N, K, group_size, clip_percentile, int4,
+                                                       static_cast<uint8_t*>(q), sw,
+                                                       static_cast<cudaStream_t>(stream)));
   return cuda_status(cider::launch_quant_weight(w, N, K, group_size, int4,
                                                 static_cast<uint8_t*>(q), sw,
                                                 static_cast<cudaStream_t>(stream)));
 }
+
+bool valid_percentile(double p) { return p > 0.0 && p <= 100.0; }   // false for NaN
 
 }  // namespace
 
@@ -214,13 +221,13 @@ cider_status_t validate_linear(const LinearArgs& a) {
   if (a.M < 0 || a.N < 0 || a.K < 0) return CIDER_ERR_INVALID_ARGUMENT;
   if (a.M > kMaxDim || a.N > kMaxDim) return CIDER_ERR_INVALID_ARGUMENT;
   const bool prequant = a.x == nullptr;
-  if (prequant ? (!a.qa || (a.mode == kEpiY && !a.sa)) : false)
+  if (prequant ? (!a.qa || (a.mode != kEpiAcc && !a.sa)) : false)
     return CIDER_ERR_INVALID_ARGUMENT;
   if (!a.w) return CIDER_ERR_INVALID_ARGUMENT;
-  if (a.mode == kEpiY && (!a.sw || !a.y)) return CIDER_ERR_INVALID_ARGUMENT;
+  if (a.mode != kEpiAcc && (!a.sw || !a.y)) return CIDER_ERR_INVALID_ARGUMENT;
   if (a.mode == kEpiAcc && !a.acc) return CIDER_ERR_INVALID_ARGUMENT;
   if (!valid_k(a.K) || a.N % 8 != 0) return CIDER_ERR_INVALID_ARGUMENT;
-  if (a.mode == kEpiY) {
+  if (a.mode != kEpiAcc) {
     if (!valid_grouping(a.granularity, a.group_size, a.K)) return CIDER_ERR_INVALID_ARGUMENT;
   } else {
     if (!(a.group_size == 0 || ((a.group_size == 64 || a.group_size == 128) && a.K % a.group_size == 0)))
@@ -237,7 +244,8 @@ cider_status_t validate_linear(const LinearArgs& a) {
 size_t linear_required_scratch(const LinearArgs& a) {
   if (a.M <= 0 || a.N <= 0 || a.K <= 0) return 0;
   if (gemv_fits(a.M, a.K)) {
-    const bool quantize_first = a.x && (a.x_bf16 || !gemv_quantizes_itself(a.M, a.K));
+    const bool quantize_first =
+        a.x && (a.x_bf16 || a.mode == kEpiYb || !gemv_quantizes_itself(a.M, a.K));
     return quantize_first ? round_up(static_cast<size_t>(a.M * a.K), 256) + round_up(4 * a.M, 256)
                           : 0;
   }
@@ -259,8 +267,10 @@ cider_status_t run_linear(const LinearArgs& a, ScratchSource& scratch) {
     // (every CTA repeats that work, cheaper than a second launch for so few
     // values); otherwise one quantization kernel writes the int8 codes first.
     // bf16 rows, and problems whose K is split over several CTAs per row
-    // block, always take the quantization kernel.  The K split's partial sums
-    // are optional scratch: without room for them the row blocks stay whole.
+    // block, always take the quantization kernel, as do bf16 outputs (the
+    // kernel that quantizes its own rows writes fp16).  The K split's partial
+    // sums are optional scratch: without room for them the row blocks stay
+    // whole.
     const size_t qs_bytes = round_up(static_cast<size_t>(a.M * a.K), 256) + round_up(4 * a.M, 256);
     size_t pbytes = gemv_part_bytes(a.M, a.N, a.K, a.int4, gs, a.mode, sms);
     if (pbytes > 0 && !scratch.fits((a.x ? qs_bytes : 0) + round_up(pbytes, 256))) pbytes = 0;
@@ -269,7 +279,7 @@ cider_status_t run_linear(const LinearArgs& a, ScratchSource& scratch) {
     const float* sa = a.sa;
     void* part = nullptr;
     const bool quantize_first =
-        a.x && (a.x_bf16 || pbytes > 0 || !gemv_quantizes_itself(a.M, a.K));
+        a.x && (a.x_bf16 || a.mode == kEpiYb || pbytes > 0 || !gemv_quantizes_itself(a.M, a.K));
     const size_t qbytes = quantize_first ? round_up(static_cast<size_t>(a.M * a.K), 256) : 0;
     const size_t sbytes = quantize_first ? round_up(4 * a.M, 256) : 0;
     if (qbytes + sbytes + pbytes > 0) {
@@ -399,10 +409,27 @@ cider_status_t cider_quantize_weight_int4(const float* w, int64_t N, int64_t K, 
   return guarded([&] { return quantize_weight(w, N, K, group_size, qw_packed, sw, true, stream); });
 }
 
+cider_status_t cider_quantize_weight_int8_clip(const float* w, int64_t N, int64_t K,
+                                               int group_size, double clip_percentile, int8_t* qw,
+                                               float* sw, void* stream) {
+  if (!valid_percentile(clip_percentile)) return CIDER_ERR_INVALID_ARGUMENT;
+  return guarded(
+      [&] { return quantize_weight(w, N, K, group_size, qw, sw, false, stream, clip_percentile); });
+}
+
+cider_status_t cider_quantize_weight_int4_clip(const float* w, int64_t N, int64_t K,
+                                               int group_size, double clip_percentile,
+                                               uint8_t* qw_packed, float* sw, void* stream) {
+  if (!valid_percentile(clip_percentile)) return CIDER_ERR_INVALID_ARGUMENT;
+  return guarded([&] {
+    return quantize_weight(w, N, K, group_size, qw_packed, sw, true, stream, clip_percentile);
+  });
+}
+
 static cider_status_t linear_entry(const void* x, const int8_t* qa, const float* sa, int64_t M,
                                    int64_t N, int64_t K, const void* w, bool int4, const float* sw,
                                    int granularity, int group_size, void* y, void* stream,
-                                   bool x_bf16 = false) {
+                                   bool x_bf16 = false, bool y_bf16 = false) {
   return guarded([&] {
     cider::LinearArgs a;
     a.x = x;
@@ -418,7 +445,7 @@ static cider_status_t linear_entry(const void* x, const int8_t* qa, const float*
     a.granularity = granularity;
     a.group_size = group_size;
     a.y = y;
-    a.mode = cider::kEpiY;
+    a.mode = y_bf16 ? cider::kEpiYb : cider::kEpiY;
     a.st = static_cast<cudaStream_t>(stream);
     if (M == 0 || N == 0) return CIDER_OK;
     if (!x && !qa) return CIDER_ERR_INVALID_ARGUMENT;
@@ -456,6 +483,26 @@ cider_status_t cider_w4a8_linear_bf16(const void* x, int64_t M, int64_t N, int64
   if (x == nullptr && M != 0 && N != 0) return CIDER_ERR_INVALID_ARGUMENT;
   return linear_entry(x, nullptr, nullptr, M, N, K, qw_packed, true, sw, granularity, group_size, y,
                       stream, true);
+}
+
+cider_status_t cider_w8a8_linear_ex(const void* x, int x_dtype, int64_t M, int64_t N, int64_t K,
+                                    const int8_t* qw, const float* sw, int granularity,
+                                    int group_size, void* y, int y_dtype, void* stream) {
+  if (x == nullptr && M != 0 && N != 0) return CIDER_ERR_INVALID_ARGUMENT;
+  if ((x_dtype != CIDER_F16 && x_dtype != CIDER_BF16) || (y_dtype != CIDER_F16 && y_dtype != CIDER_BF16))
+    return CIDER_ERR_INVALID_ARGUMENT;
+  return linear_entry(x, nullptr, nullptr, M, N, K, qw, false, sw, granularity, group_size, y,
+                      stream, x_dtype == CIDER_BF16, y_dtype == CIDER_BF16);
+}
+
+cider_status_t cider_w4a8_linear_ex(const void* x, int x_dtype, int64_t M, int64_t N, int64_t K,
+                                    const uint8_t* qw_packed, const float* sw, int granularity,
+                                    int group_size, void* y, int y_dtype, void* stream) {
+  if (x == nullptr && M != 0 && N != 0) return CIDER_ERR_INVALID_ARGUMENT;
+  if ((x_dtype != CIDER_F16 && x_dtype != CIDER_BF16) || (y_dtype != CIDER_F16 && y_dtype != CIDER_BF16))
+    return CIDER_ERR_INVALID_ARGUMENT;
+  return linear_entry(x, nullptr, nullptr, M, N, K, qw_packed, true, sw, granularity, group_size,
+                      y, stream, x_dtype == CIDER_BF16, y_dtype == CIDER_BF16);
 }
 
 cider_status_t cider_w8a8_linear_prequant(const int8_t* qa, const float* sa, int64_t M, int64_t N,

@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -404,6 +405,15 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
+}
+
+// ---------------------------------------------------------------- outputs
+// The bits of one output value: the fp32 result rounded once to fp16 or to
+// bf16 (round to nearest even either way).
+template <bool BF16>
+__device__ __forceinline__ uint16_t y_bits(float v) {
+  if constexpr (BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  return __half_as_ushort(__float2half_rn(v));
 }
 
 // ---------------------------------------------------------------- exact integer -> fp16

@@ -40,6 +40,7 @@ inline cudaError_t ensure_max_dynamic_smem(const void* kern, int bytes,
 enum EpiMode : int {
   kEpiY = 0,    // dequantize and store fp16 y [M, N]
   kEpiAcc = 1,  // store the exact int32 accumulators [M, N, G]
+  kEpiYb = 2,   // dequantize and store bf16 y [M, N]
 };
 
 // quant.cu
@@ -57,6 +58,10 @@ cudaError_t launch_quant_act_f16_from_bf16(const __nv_bfloat16* x, int64_t M, in
                                            cudaStream_t st);
 cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int group_size, bool int4,
                                 uint8_t* q, float* sw, cudaStream_t st);
+// The same with percentile-clipped scales (clip_percentile in (0, 100]).
+cudaError_t launch_quant_weight_clip(const float* w, int64_t N, int64_t K, int group_size,
+                                     double clip_percentile, bool int4, uint8_t* q, float* sw,
+                                     cudaStream_t st);
 // Offset-binary INT4 bytes -> two's complement INT4 bytes (src may equal dst).
 cudaError_t launch_int4_from_offset(const uint8_t* src, uint8_t* dst, int64_t nbytes,
                                     cudaStream_t st);

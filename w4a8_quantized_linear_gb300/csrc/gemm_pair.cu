@@ -187,17 +187,17 @@ __device__ __forceinline__ bool pair_tile_fast(const PairArgs& a, int mt, int la
   return mx <= a.l1_limit;
 }
 
-// y[m, n0 .. n0 + 7] = fp16((acc * s_a[m]) * s_w[n]) from eight exact
-// accumulator values and the eight weight scales, one 16-byte store.
+// y[m, n0 .. n0 + 7] = round((acc * s_a[m]) * s_w[n]) to fp16 (or bf16) from
+// eight exact accumulator values and the eight weight scales, one 16-byte store.
+template <bool BF16>
 __device__ __forceinline__ void store8_y(const PairArgs& p, int m, float sam, int n0, const float* f,
                                          const float (&w)[8]) {
   uint32_t h[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const __half lo = __float2half_rn(__fmul_rn(__fmul_rn(f[2 * i], sam), w[2 * i]));
-    const __half hi = __float2half_rn(__fmul_rn(__fmul_rn(f[2 * i + 1], sam), w[2 * i + 1]));
-    h[i] = static_cast<uint32_t>(__half_as_ushort(lo)) |
-           (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+    const uint32_t lo = y_bits<BF16>(__fmul_rn(__fmul_rn(f[2 * i], sam), w[2 * i]));
+    const uint32_t hi = y_bits<BF16>(__fmul_rn(__fmul_rn(f[2 * i + 1], sam), w[2 * i + 1]));
+    h[i] = lo | (hi << 16);
   }
   *reinterpret_cast<uint4*>(p.y + static_cast<int64_t>(m) * p.N + n0) =
       make_uint4(h[0], h[1], h[2], h[3]);
@@ -467,7 +467,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       const int row = q * 32 + lane;   // token of this thread within the CTA's 128
       const int m = mt * kPTileM + static_cast<int>(rank) * kPHalf + row;
       const bool mvalid = m < p.M;
-      const float sam = (EPI == kEpiY && mvalid) ? __ldg(p.sa + m) : 0.0f;
+      const float sam = (EPI != kEpiAcc && mvalid) ? __ldg(p.sa + m) : 0.0f;
       const int n_tile = nt * kPTileN;
       const bool piece = u.kind == kUnitPiece;
       // partial slot of a pair: 16-byte column group j of this thread's token
@@ -483,7 +483,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int n = n_tile + lane * 8 + i;
-        swr[i] = (EPI == kEpiY && n < p.N) ? __ldg(p.sw + n) : 0.0f;
+        swr[i] = (EPI != kEpiAcc && n < p.N) ? __ldg(p.sw + n) : 0.0f;
       }
       // scales of tile columns col .. col + 7 (col % 8 == 0); the whole warp calls this
       auto scales8 = [&](int col, float (&w)[8]) {
@@ -500,7 +500,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           float f[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) f[i] = __int2float_rn(iv[i]);
-          store8_y(p, m, sam, n0, f, w);
+          store8_y<EPI == kEpiYb>(p, m, sam, n0, f, w);
         }
       };
       // eight exact accumulator values of tile columns col .. col + 7: the
@@ -515,7 +515,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           }
         } else {
           float w[8];
-          if (EPI == kEpiY) scales8(col, w);
+          if (EPI != kEpiAcc) scales8(col, w);
           if (mvalid && n0 < p.N) store8(n0, iv, w);
         }
       };
@@ -623,7 +623,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             if (2 * g < nj) {   // warp-uniform
               const int col = (jb + 2 * g) * 4;
               float w[8];
-              if (EPI == kEpiY) scales8(col, w);
+              if (EPI != kEpiAcc) scales8(col, w);
               int iv[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) iv[i] = sum[8 * g + i];
@@ -860,10 +860,12 @@ cudaError_t launch_gemm_pair(const __half* qa16, const float* sa, const int* row
   e = device_error_word(&a.err);
   if (e != cudaSuccess) return e;
   if (int4)
-    return mode == kEpiY ? launch_pair<true, kEpiY>(tmX, tmW, a, pl.clusters, st)
-                         : launch_pair<true, kEpiAcc>(tmX, tmW, a, pl.clusters, st);
-  return mode == kEpiY ? launch_pair<false, kEpiY>(tmX, tmW, a, pl.clusters, st)
-                       : launch_pair<false, kEpiAcc>(tmX, tmW, a, pl.clusters, st);
+    return mode == kEpiY    ? launch_pair<true, kEpiY>(tmX, tmW, a, pl.clusters, st)
+           : mode == kEpiYb ? launch_pair<true, kEpiYb>(tmX, tmW, a, pl.clusters, st)
+                            : launch_pair<true, kEpiAcc>(tmX, tmW, a, pl.clusters, st);
+  return mode == kEpiY    ? launch_pair<false, kEpiY>(tmX, tmW, a, pl.clusters, st)
+         : mode == kEpiYb ? launch_pair<false, kEpiYb>(tmX, tmW, a, pl.clusters, st)
+                          : launch_pair<false, kEpiAcc>(tmX, tmW, a, pl.clusters, st);
 }
 
 }  // namespace cider

@@ -334,7 +334,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
             }
         }
       }
-    } else if (EPI == kEpiY) {
+    } else if (EPI != kEpiAcc) {
       // ---------------------------------------------------------- weight-scale loader
       int f = 0;   // (tile, group) units of this pair, in drain order
       for (int tile = cid; tile < p.num_tiles; tile += nclusters) {
@@ -443,7 +443,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
       for (int g = 0; g < p.G; ++g, ++ch) {
         const int b = ch & 1;
         const int js = ch % kGSwSlots;
-        if (EPI == kEpiY && !__all_sync(0xffffffffu, mbar_sleep_bounded(
+        if (EPI != kEpiAcc && !__all_sync(0xffffffffu, mbar_sleep_bounded(
                                                          swf_bar(js), (ch / kGSwSlots) & 1,
                                                          abort_flag, err, kGWaitNs)))
           goto done;
@@ -472,7 +472,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const int c = 2 * c2 + hh;   // 16-column chunk of the warp's 128
-            if (EPI == kEpiY) {
+            if (EPI != kEpiAcc) {
 #pragma unroll
               for (int j4 = 0; j4 < 4; ++j4) {
                 const float4 w = w4[c * 4 + j4];
@@ -495,12 +495,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
             }
           }
         }
-        if (EPI == kEpiY) {
+        if (EPI != kEpiAcc) {
           __syncwarp();
           if (lane == 0) mbar_arrive(swe_bar(js));   // this warp is done with the slot's scales
         }
       }
-      if (EPI == kEpiY && mvalid) {
+      if (EPI != kEpiAcc && mvalid) {
         const float sam = __ldg(p.sa + m);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
@@ -509,10 +509,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
             uint32_t hw[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const __half lo = __float2half_rn(__fmul_rn(fsum[8 * c + 2 * i], sam));
-              const __half hi = __float2half_rn(__fmul_rn(fsum[8 * c + 2 * i + 1], sam));
-              hw[i] = static_cast<uint32_t>(__half_as_ushort(lo)) |
-                      (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+              const uint32_t lo = y_bits<EPI == kEpiYb>(__fmul_rn(fsum[8 * c + 2 * i], sam));
+              const uint32_t hi = y_bits<EPI == kEpiYb>(__fmul_rn(fsum[8 * c + 2 * i + 1], sam));
+              hw[i] = lo | (hi << 16);
             }
             *reinterpret_cast<uint4*>(p.y + static_cast<int64_t>(m) * p.N + n) =
                 make_uint4(hw[0], hw[1], hw[2], hw[3]);
@@ -637,10 +636,12 @@ cudaError_t launch_gemm_pg(const __half* qa16, const float* sa, int64_t M, int64
   if (e != cudaSuccess) return e;
   const int clusters = a.num_tiles < nc ? a.num_tiles : nc;
   if (int4)
-    return mode == kEpiY ? launch_pg<true, kEpiY>(tmX, tmW, a, clusters, st)
-                         : launch_pg<true, kEpiAcc>(tmX, tmW, a, clusters, st);
-  return mode == kEpiY ? launch_pg<false, kEpiY>(tmX, tmW, a, clusters, st)
-                       : launch_pg<false, kEpiAcc>(tmX, tmW, a, clusters, st);
+    return mode == kEpiY    ? launch_pg<true, kEpiY>(tmX, tmW, a, clusters, st)
+           : mode == kEpiYb ? launch_pg<true, kEpiYb>(tmX, tmW, a, clusters, st)
+                            : launch_pg<true, kEpiAcc>(tmX, tmW, a, clusters, st);
+  return mode == kEpiY    ? launch_pg<false, kEpiY>(tmX, tmW, a, clusters, st)
+         : mode == kEpiYb ? launch_pg<false, kEpiYb>(tmX, tmW, a, clusters, st)
+                          : launch_pg<false, kEpiAcc>(tmX, tmW, a, clusters, st);
 }
 
 }  // namespace cider

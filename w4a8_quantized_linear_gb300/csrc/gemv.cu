@@ -383,7 +383,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             else if (ks > 1)
               p.part[(static_cast<int64_t>(slice) * M + m) * N + n] = static_cast<uint32_t>(v);
             else
-              p.y[off] = __float2half_rn(__fmul_rn(__fmul_rn(__int2float_rn(v), s_sa[m]), __ldg(p.sw + n)));
+              reinterpret_cast<uint16_t*>(p.y)[off] = y_bits<EPI == kEpiYb>(
+                  __fmul_rn(__fmul_rn(__int2float_rn(v), s_sa[m]), __ldg(p.sw + n)));
           } else {
             float v = 0.0f;
 #pragma unroll
@@ -391,7 +392,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             if (ks > 1)
               p.part[(static_cast<int64_t>(slice) * M + m) * N + n] = __float_as_uint(v);
             else
-              p.y[off] = __float2half_rn(v);
+              reinterpret_cast<uint16_t*>(p.y)[off] = y_bits<EPI == kEpiYb>(v);
           }
         }
       }
@@ -437,7 +438,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         }
       }
       const int g = PG ? (c * VALS) / p.gs : 0;
-      const float swg = (PG && EPI == kEpiY && live && nvalid) ? __ldg(p.sw + n * p.G + g) : 0.0f;
+      const float swg = (PG && EPI != kEpiAcc && live && nvalid) ? __ldg(p.sw + n * p.G + g) : 0.0f;
 #pragma unroll
       for (int m = 0; m < MB; ++m) {
         uint4 a0 = make_uint4(0u, 0u, 0u, 0u), a1 = a0;
@@ -460,7 +461,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         }
         if (!PG) {
           acc[m] = pv;
-        } else if (EPI == kEpiY) {
+        } else if (EPI != kEpiAcc) {
           fs[m] = fmaf(swg, static_cast<float>(pv), fs[m]);
         } else {
           // exact per-group accumulators: reduce the lanes of each group (a
@@ -495,10 +496,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         } else if (ks > 1) {
           p.part[(static_cast<int64_t>(slice) * M + m) * N + n] = bits;
         } else if (!PG) {
-          p.y[off] = __float2half_rn(
+          reinterpret_cast<uint16_t*>(p.y)[off] = y_bits<EPI == kEpiYb>(
               __fmul_rn(__fmul_rn(__int2float_rn(static_cast<int>(bits)), s_sa[m]), __ldg(p.sw + n)));
         } else {
-          p.y[off] = __float2half_rn(__fmul_rn(__uint_as_float(bits), s_sa[m]));
+          reinterpret_cast<uint16_t*>(p.y)[off] =
+              y_bits<EPI == kEpiYb>(__fmul_rn(__uint_as_float(bits), s_sa[m]));
         }
       }
     }
@@ -516,7 +518,7 @@ int ring_slots(int64_t MB, int64_t K, bool mma = false) {
 // Partial sums of the K slices -> y: per channel the exact int32 sum, then
 // (acc * s_a) * s_w; per group the fp32 sum of the slices' partials, times
 // s_a unless the partials already carry it (tensor-core form).
-template <bool PG, bool PG_SCALED>
+template <bool PG, bool PG_SCALED, bool BF16>
 __global__ void __launch_bounds__(256) gemv_combine_kernel(const uint32_t* __restrict__ part,
                                                            int ks, int M, int64_t N,
                                                            const float* __restrict__ sa,
@@ -530,11 +532,12 @@ __global__ void __launch_bounds__(256) gemv_combine_kernel(const uint32_t* __res
     if (!PG) {
       int v = 0;
       for (int s = 0; s < ks; ++s) v += static_cast<int>(part[s * total + i]);
-      y[i] = __float2half_rn(__fmul_rn(__fmul_rn(__int2float_rn(v), __ldg(sa + m)), __ldg(sw + n)));
+      reinterpret_cast<uint16_t*>(y)[i] =
+          y_bits<BF16>(__fmul_rn(__fmul_rn(__int2float_rn(v), __ldg(sa + m)), __ldg(sw + n)));
     } else {
       float v = 0.0f;
       for (int s = 0; s < ks; ++s) v += __uint_as_float(part[s * total + i]);
-      y[i] = __float2half_rn(PG_SCALED ? v : __fmul_rn(v, __ldg(sa + m)));
+      reinterpret_cast<uint16_t*>(y)[i] = y_bits<BF16>(PG_SCALED ? v : __fmul_rn(v, __ldg(sa + m)));
     }
   }
 }
@@ -651,7 +654,7 @@ cudaError_t launch_one(const __half* x, const int8_t* qa, const float* sa, int64
   if (e != cudaSuccess || sp.ks == 1) return e;
   const int64_t total = M * N;
   const unsigned cb = static_cast<unsigned>((total + 255) / 256 < 1024 ? (total + 255) / 256 : 1024);
-  gemv_combine_kernel<PG, PG && MMA><<<cb, 256, 0, st>>>(part, sp.ks, static_cast<int>(M), N, sa,
+  gemv_combine_kernel<PG, PG && MMA, EPI == kEpiYb><<<cb, 256, 0, st>>>(part, sp.ks, static_cast<int>(M), N, sa,
                                                          sw, y);
   return cudaGetLastError();
 }
@@ -670,7 +673,7 @@ cudaError_t dispatch_mb(const __half* x, const int8_t* qa, const float* sa, int6
   const bool fq = x != nullptr;
   constexpr bool kMmaMB = MB >= 4;
   const bool mma = gemv_uses_mma(MB, K, pg, mode);
-  const GemvSplit sp = gemv_plan(MB, N, K, int4, mma, part != nullptr && !fq && mode == kEpiY,
+  const GemvSplit sp = gemv_plan(MB, N, K, int4, mma, part != nullptr && !fq && mode != kEpiAcc,
                                  num_sms);
   if (kMmaMB && mma) {
 #define CIDER_GEMV_MMA_CASE(I4, P, E, F)                                                      \
@@ -687,6 +690,10 @@ cudaError_t dispatch_mb(const __half* x, const int8_t* qa, const float* sa, int6
     CIDER_GEMV_MMA_CASE(true, false, kEpiY, false)
     CIDER_GEMV_MMA_CASE(true, true, kEpiY, false)
     CIDER_GEMV_MMA_CASE(true, false, kEpiAcc, false)
+    CIDER_GEMV_MMA_CASE(false, false, kEpiYb, false)
+    CIDER_GEMV_MMA_CASE(false, true, kEpiYb, false)
+    CIDER_GEMV_MMA_CASE(true, false, kEpiYb, false)
+    CIDER_GEMV_MMA_CASE(true, true, kEpiYb, false)
 #undef CIDER_GEMV_MMA_CASE
   }
 #define CIDER_GEMV_CASE(I4, P, E, F)                                                          \
@@ -705,6 +712,10 @@ cudaError_t dispatch_mb(const __half* x, const int8_t* qa, const float* sa, int6
   CIDER_GEMV_CASE(true, true, kEpiY, false)
   CIDER_GEMV_CASE(true, false, kEpiAcc, false)
   CIDER_GEMV_CASE(true, true, kEpiAcc, false)
+  CIDER_GEMV_CASE(false, false, kEpiYb, false)
+  CIDER_GEMV_CASE(false, true, kEpiYb, false)
+  CIDER_GEMV_CASE(true, false, kEpiYb, false)
+  CIDER_GEMV_CASE(true, true, kEpiYb, false)
 #undef CIDER_GEMV_CASE
   return cudaErrorInvalidValue;
 }
@@ -720,7 +731,7 @@ bool gemv_fits(int64_t M, int64_t K) {
 
 int gemv_slices(int64_t M, int64_t N, int64_t K, bool int4, int group_size, int mode,
                 int num_sms) {
-  if (mode != kEpiY) return 1;
+  if (mode == kEpiAcc) return 1;
   int64_t mb = 1;
   while (mb < M) mb *= 2;
   return gemv_plan(mb, N, K, int4, gemv_uses_mma(mb, K, group_size > 0, mode), true, num_sms).ks;

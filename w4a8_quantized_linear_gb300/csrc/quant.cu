@@ -12,6 +12,7 @@
 // the README's roadmap); both widen to fp32 exactly before the same steps.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <math.h>
 #include <stdint.h>
 
 #include <type_traits>
@@ -278,6 +279,160 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const float* __restri
   }
 }
 
+// ---------------------------------------------------------------- clipped weight scales
+// Percentile-clipped weight scales (Cider README, "Notes": min-max scales by
+// default, or a percentile, clip_percentile = 99.9).  For a block of n
+// values, the clip is the p-th percentile of |W| with linear interpolation
+// between the order statistics lo and hi = lo + 1 at the fractional rank
+// (n - 1) p / 100 (lo, hi and the weight t come from the host, in double);
+// clip = a_lo + t (a_hi - a_lo) in fp32 without FMA, s = clip / qmax (1 when
+// clip == 0), and codes clamp as for min-max scales.
+
+// Scale and codes of one block given its clip value; `src` holds the block's
+// bs values, element pairs (2j, 2j + 1) go to lanes / threads j (mod `step`).
+template <bool INT4>
+__device__ __forceinline__ float clipped_scale(float alo, float ahi, float t) {
+  const float clip = __fadd_rn(alo, __fmul_rn(t, __fsub_rn(ahi, alo)));
+  return (clip == 0.0f) ? 1.0f : __fdiv_rn(clip, INT4 ? 7.0f : 127.0f);
+}
+
+template <bool INT4>
+__device__ __forceinline__ void store_block_codes(const float* src, int64_t bs, float s, int64_t first,
+                                                  int64_t step, uint8_t* q_row, int64_t off) {
+  const float qmin = INT4 ? -8.0f : -127.0f;
+  const float qmax = INT4 ? 7.0f : 127.0f;
+  const float2* src2 = reinterpret_cast<const float2*>(src);
+  for (int64_t j = first; j < bs / 2; j += step) {
+    const float2 v = src2[j];
+    const int c0 = static_cast<int>(fminf(fmaxf(rintf(__fdiv_rn(v.x, s)), qmin), qmax));
+    const int c1 = static_cast<int>(fminf(fmaxf(rintf(__fdiv_rn(v.y, s)), qmin), qmax));
+    if (INT4) {
+      q_row[off / 2 + j] = static_cast<uint8_t>((c0 & 0xF) | ((c1 & 0xF) << 4));
+    } else {
+      *reinterpret_cast<uint16_t*>(q_row + off + 2 * j) =
+          static_cast<uint16_t>((c0 & 0xFF) | ((c1 & 0xFF) << 8));
+    }
+  }
+}
+
+// Per group (GS = 64 or 128 values): one warp per block.  Each element's
+// rank is the number of block values below it (ties broken by position), so
+// exactly one element has each rank.
+template <bool INT4, int GS>
+__global__ void __launch_bounds__(256) quant_weight_clip_group_kernel(
+    const float* __restrict__ w, int64_t N, int64_t K, int64_t G, int lo, int hi, float t,
+    uint8_t* __restrict__ q, float* __restrict__ sw) {
+  constexpr int PER = GS / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t blk = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (blk >= N * G) return;   // uniform per warp
+  const int64_t n = blk / G, g = blk % G;
+  const float* src = w + n * K + g * GS;
+  float v[PER];
+  int rank[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    v[j] = fabsf(src[lane + 32 * j]);
+    rank[j] = 0;
+  }
+#pragma unroll
+  for (int j2 = 0; j2 < PER; ++j2)
+    for (int l = 0; l < 32; ++l) {
+      const float o = __shfl_sync(0xffffffffu, v[j2], l);
+      const int oi = l + 32 * j2;
+#pragma unroll
+      for (int j = 0; j < PER; ++j)
+        rank[j] += (o < v[j] || (o == v[j] && oi < lane + 32 * j)) ? 1 : 0;
+    }
+  float alo = -1.0f, ahi = -1.0f;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    if (rank[j] == lo) alo = v[j];
+    if (rank[j] == hi) ahi = v[j];
+  }
+  alo = warp_max(alo);
+  ahi = warp_max(ahi);
+  const float s = clipped_scale<INT4>(alo, ahi, t);
+  if (lane == 0) sw[n * G + g] = s;
+  store_block_codes<INT4>(src, GS, s, lane, 32, q + n * (INT4 ? K / 2 : K), g * GS);
+}
+
+// Per channel (a whole row of K values): one CTA per row; a radix select over
+// the bit patterns of |w| (non-negative floats order like unsigned integers),
+// 8 bits per pass, finds the value of rank lo; the value of rank hi is the
+// same when more than lo + 1 values are <= it, else the smallest value above.
+constexpr int kClipThreads = 256;
+
+template <bool INT4>
+__global__ void __launch_bounds__(kClipThreads) quant_weight_clip_row_kernel(
+    const float* __restrict__ w, int64_t K, int64_t lo, int64_t hi, float t,
+    uint8_t* __restrict__ q, float* __restrict__ sw) {
+  __shared__ unsigned hist[256];
+  __shared__ uint32_t s_bucket;
+  __shared__ unsigned long long s_rest;
+  __shared__ unsigned long long s_cnt[kClipThreads / 32];
+  __shared__ uint32_t s_min[kClipThreads / 32];
+  const int64_t n = blockIdx.x;
+  const uint32_t* row = reinterpret_cast<const uint32_t*>(w + n * K);
+  uint32_t prefix = 0u, mask = 0u;
+  unsigned long long k = static_cast<unsigned long long>(lo);
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += kClipThreads) hist[i] = 0u;
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < K; i += kClipThreads) {
+      const uint32_t b = row[i] & 0x7FFFFFFFu;
+      if ((b & mask) == prefix) atomicAdd(&hist[(b >> shift) & 0xFFu], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned long long cum = 0;
+      uint32_t d = 0;
+      for (; d < 255u; ++d) {
+        if (cum + hist[d] > k) break;
+        cum += hist[d];
+      }
+      s_bucket = d;
+      s_rest = k - cum;
+    }
+    __syncthreads();
+    prefix |= s_bucket << shift;
+    mask |= 0xFFu << shift;
+    k = s_rest;
+    __syncthreads();
+  }
+  const float alo = __uint_as_float(prefix);
+  float ahi = alo;
+  if (hi != lo) {
+    unsigned long long le = 0;
+    uint32_t above = 0xFFFFFFFFu;
+    for (int64_t i = threadIdx.x; i < K; i += kClipThreads) {
+      const uint32_t b = row[i] & 0x7FFFFFFFu;
+      if (b <= prefix) ++le;
+      else above = min(above, b);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      le += __shfl_xor_sync(0xffffffffu, le, o);
+      above = min(above, __shfl_xor_sync(0xffffffffu, above, o));
+    }
+    if ((threadIdx.x & 31) == 0) {
+      s_cnt[threadIdx.x >> 5] = le;
+      s_min[threadIdx.x >> 5] = above;
+    }
+    __syncthreads();
+    le = 0;
+    above = 0xFFFFFFFFu;
+    for (int i = 0; i < kClipThreads / 32; ++i) {
+      le += s_cnt[i];
+      above = min(above, s_min[i]);
+    }
+    if (le <= static_cast<unsigned long long>(lo) + 1) ahi = __uint_as_float(above);
+  }
+  const float s = clipped_scale<INT4>(alo, ahi, t);
+  if (threadIdx.x == 0) sw[n] = s;
+  store_block_codes<INT4>(w + n * K, K, s, threadIdx.x, kClipThreads, q + n * (INT4 ? K / 2 : K), 0);
+}
+
 // int8 codes -> the same codes as fp16 integers (exact), one CTA per row,
 // plus the row's sum of |code|.
 __global__ void __launch_bounds__(kQuantThreads) codes_s8_to_f16_kernel(const int8_t* __restrict__ qa,
@@ -377,6 +532,43 @@ cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int group_
     quant_weight_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, st>>>(w, N, K, bs, G, q, sw);
   else
     quant_weight_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(w, N, K, bs, G, q, sw);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_weight_clip(const float* w, int64_t N, int64_t K, int group_size,
+                                     double clip_percentile, bool int4, uint8_t* q, float* sw,
+                                     cudaStream_t st) {
+  const int64_t bs = group_size > 0 ? group_size : K;
+  const int64_t G = K / bs;
+  // fractional rank of the percentile in a block of bs values (in double, as
+  // the definition states), its two order statistics and the fp32 weight
+  const double h = static_cast<double>(bs - 1) * clip_percentile / 100.0;
+  int64_t lo = static_cast<int64_t>(floor(h));
+  if (lo > bs - 1) lo = bs - 1;
+  const int64_t hi = lo + 1 < bs ? lo + 1 : bs - 1;
+  const float t = static_cast<float>(h - static_cast<double>(lo));
+  if (group_size == 0) {
+    if (int4)
+      quant_weight_clip_row_kernel<true><<<static_cast<unsigned>(N), kClipThreads, 0, st>>>(
+          w, K, lo, hi, t, q, sw);
+    else
+      quant_weight_clip_row_kernel<false><<<static_cast<unsigned>(N), kClipThreads, 0, st>>>(
+          w, K, lo, hi, t, q, sw);
+    return cudaGetLastError();
+  }
+  const unsigned blocks = static_cast<unsigned>((N * G + 7) / 8);
+  const int l = static_cast<int>(lo), h2 = static_cast<int>(hi);
+  if (group_size == 64) {
+    if (int4)
+      quant_weight_clip_group_kernel<true, 64><<<blocks, 256, 0, st>>>(w, N, K, G, l, h2, t, q, sw);
+    else
+      quant_weight_clip_group_kernel<false, 64><<<blocks, 256, 0, st>>>(w, N, K, G, l, h2, t, q, sw);
+  } else {
+    if (int4)
+      quant_weight_clip_group_kernel<true, 128><<<blocks, 256, 0, st>>>(w, N, K, G, l, h2, t, q, sw);
+    else
+      quant_weight_clip_group_kernel<false, 128><<<blocks, 256, 0, st>>>(w, N, K, G, l, h2, t, q, sw);
+  }
   return cudaGetLastError();
 }
 
