@@ -282,9 +282,27 @@ def run_reference(a):
                        "group_size": a.gs, "bits": a.bits,
                        "note": "CPU oracle; each step computes a row sample of the workload"},
             "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "host": host_cpu(), "sample": sample},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def host_cpu() -> dict:
+    """The host's logical CPU count and model name (for the CPU baseline)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model", "processor name") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:
+        import platform
+        model = platform.processor() or platform.machine()
+    return {"nproc": os.cpu_count(), "cpu_model": model}
 
 
 def cpu_baseline(a, x, qv, sw, budget_s=12.0):
@@ -299,7 +317,7 @@ def cpu_baseline(a, x, qv, sw, budget_s=12.0):
         rows = min(rows + chunk, a.M)
         el = time.perf_counter() - t
     val = 2.0 * rows * a.N * a.K / el / 1e12
-    return {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "host": host_cpu(),
             "sample": f"rows 0..{rows - 1} of the {workload_name(a)} workload "
                       f"({rows} x {a.N} x {a.K}), single-threaded C oracle, {el:.1f} s"}
 

@@ -279,6 +279,16 @@ cider_status_t cider_w8a8_linear_noalloc(const void* x, int64_t M, int64_t N,
 cider_status_t cider_timing_begin(int64_t capacity);
 cider_status_t cider_timing_end(int64_t* count, double* total_ms);
 
+/* Scratch memory of the library's per-device pool: every linear takes its
+ * scratch (activation codes and scales, work-split partial sums) from a
+ * stream-ordered pool on the current device that keeps freed blocks for the
+ * next calls, so the pool holds as much as the largest call so far needed
+ * (e.g. ~200 MB for M = 8192, K = 12288).  This call synchronizes `stream`
+ * and returns pool memory beyond `keep_bytes` to the device (the next larger
+ * call allocates again).  CIDER_ERR_INVALID_ARGUMENT for keep_bytes < 0;
+ * CIDER_OK when the pool was never used on this device. */
+cider_status_t cider_trim_scratch_pool(int64_t keep_bytes, void* stream);
+
 /* Device-side error word shared by the library's kernels on the current
  * device.  Every wait inside a kernel is bounded; a wait that runs out sets
  * this word and the kernel returns early instead of hanging.  This call

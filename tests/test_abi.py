@@ -191,3 +191,8 @@ def test_dtype_linears_and_clipped_quantizers_check_arguments(lib, no_device):
             assert f(P, 8, 256, 64, bad, P, P, None) == INVALID
         assert f(P, 8, 256, 96, 99.9, P, P, None) == INVALID                 # group size
         assert f(P + 1, 8, 256, 0, 99.9, P, P, None) == MISALIGNED
+
+
+def test_trim_scratch_pool_argument_checks(lib, no_device):
+    assert lib.cider_trim_scratch_pool(-1, None) == INVALID
+    assert lib.cider_trim_scratch_pool(0, None) == UNSUPPORTED

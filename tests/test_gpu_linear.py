@@ -383,3 +383,18 @@ def test_full_size_shared_activation_projection_set(cider):
         assert y.shape == (M, N)
         yref = oracle.linear(x, qw, sw, 0, rows=rows, threads=8)
         assert_bits_equal(y[rows], yref, f"Qwen3-2B {name} projection rows")
+
+
+def test_trim_scratch_pool_keeps_results(cider):
+    """Trimming the pooled scratch after a large call releases it and the
+    next calls allocate again and compute the same bits."""
+    M, N, K = 2048, 1024, 4096
+    x = to_dev(inputs.activations(M, K, seed=5))
+    qw_dev, _, sw = make_weights(N, K, 0, 8, seed=6)
+    qw_d, sw_d = to_dev(qw_dev), to_dev(sw)
+    y0 = cider.cider_w8a8_linear(x, qw_d, sw_d, 0)
+    cider.cider_trim_scratch_pool(0)
+    y1 = cider.cider_w8a8_linear(x, qw_d, sw_d, 0)
+    cider.cider_trim_scratch_pool(1 << 20)
+    assert_bits_equal(to_host(y1), to_host(y0), "after trimming the pool")
+    assert cider.cider_check_device_error() == 0

@@ -66,6 +66,7 @@ def _declare(lib):
         "cider_w8a8_accumulators": ([p, i64, i64, i64, p, i32, p, p], i32),
         "cider_w4a8_accumulators": ([p, i64, i64, i64, p, i32, p, p], i32),
         "cider_check_device_error": ([p], i32),
+        "cider_trim_scratch_pool": ([i64, p], i32),
         "cider_timing_begin": ([i64], i32),
         "cider_timing_end": ([ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)], i32),
         "cider_debug_wait_timeout": ([i64, p], i32),
@@ -320,6 +321,14 @@ def cider_check_device_error(device=None) -> int:
     the library's device error word: 0 (CIDER_OK) or 5 (CIDER_ERR_TIMEOUT)."""
     s = torch.cuda.current_stream(device)
     return int(_load().cider_check_device_error(ctypes.c_void_p(s.cuda_stream)))
+
+
+def cider_trim_scratch_pool(keep_bytes: int = 0, device=None) -> None:
+    """Return the library's pooled scratch memory beyond ``keep_bytes`` to the
+    device (after the current stream's queued calls have run)."""
+    s = torch.cuda.current_stream(device)
+    _check("cider_trim_scratch_pool",
+           _load().cider_trim_scratch_pool(int(keep_bytes), ctypes.c_void_p(s.cuda_stream)))
 
 
 def cider_debug_wait_timeout(max_polls: int, device=None) -> int:

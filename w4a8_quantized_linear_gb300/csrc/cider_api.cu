@@ -590,6 +590,26 @@ cider_status_t cider_timing_end(int64_t* count, double* total_ms) {
   });
 }
 
+cider_status_t cider_trim_scratch_pool(int64_t keep_bytes, void* stream) {
+  return guarded([&] {
+    if (keep_bytes < 0) return CIDER_ERR_INVALID_ARGUMENT;
+    int dev = 0;
+    cider_status_t s = cider::check_device(&dev, nullptr);
+    if (s != CIDER_OK) return s;
+    cudaMemPool_t pool = nullptr;
+    {
+      std::lock_guard<std::mutex> lk(g_pool_mu);
+      pool = g_pool[dev];
+    }
+    if (pool == nullptr) return CIDER_OK;   // nothing allocated on this device yet
+    // blocks freed by calls still queued on `stream` return to the pool only
+    // when those calls have run
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return cuda_status(cudaErrorUnknown);
+    return cuda_status(cudaMemPoolTrimTo(pool, static_cast<size_t>(keep_bytes)));
+  });
+}
+
 cider_status_t cider_check_device_error(void* stream) {
   return guarded([&] {
     cider_status_t s = cider::check_device(nullptr, nullptr);

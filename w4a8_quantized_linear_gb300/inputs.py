@@ -6,8 +6,10 @@ layers and wikitext2, which are not available; these stand in for them).
 
 Recipe
 ------
-* Random numbers: numpy ``Generator(PCG64(seed))``; one seed per tensor,
-  ``seed = base_seed + tensor_index`` in the fixed order x, W, x2, W2, ...
+* Random numbers: numpy ``Generator(PCG64(seed))``; one seed per tensor:
+  layer i of a workload draws its activations x with ``base_seed + 2 i`` and
+  its weights W with ``base_seed + 2 i + 1`` (tensor index 0, 1, 2, 3, ... in
+  the order x, W, x2, W2, ...).
 * Activations x [M, K]: fp32 N(0, 1); ``floor(K / 100)`` outlier channels
   (1 % of K, sampled without replacement from the same generator) are scaled
   by 20; the result is rounded to fp16 (or, for the bf16 entry points, to
