@@ -12,7 +12,8 @@
 // come from one quantization launch instead, so that each of the many CTAs
 // does not quantize the same rows again.  The producer warp issues the first
 // weight loads before that staging, so HBM streaming starts at once: weight
-// tiles of 16 rows x 256 bytes go by 2-D TMA into a ring of up to 8 slots.
+// tiles of 16 rows x 256 bytes go by 2-D TMA into a ring of up to 8 slots,
+// each slot refilled by its own lane of the producer warp.
 // Grids are sized to be resident in one wave; CTA c takes row blocks c,
 // c + grid, ...
 //
@@ -52,7 +53,7 @@ constexpr int kSmemActMax = 200 * 1024;
 constexpr int kBoxRows = 16;                         // weight rows per tile (2 per consumer warp)
 constexpr int kBoxBytes = 256;                       // weight bytes of a row per tile
 constexpr int kTileBytes = kBoxRows * kBoxBytes;     // 4 KiB
-constexpr int kRingMax = 8;
+constexpr int kRingMax = 12;
 constexpr int kStageBatch = 4;    // 16-byte activation loads in flight per thread while staging
 constexpr int kSmemBudget = 227 * 1024 - 4096;       // dynamic: leave room for static arrays
 constexpr int kRedBytes = kGemvWarps * 32 * 8 * 4;   // tensor-core form: block reduction buffer
@@ -147,12 +148,17 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 
   if (warp == kGemvWarps) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tensormap(&tmW);
+    // Lane s refills ring slot s (tiles it = s, s + NS, ...): the copies one
+    // thread issues complete one after another (~0.45 us per 4 KB tile on
+    // GB300, however many are in flight), so each slot gets its own issuer.
+    if (lane == 0) prefetch_tensormap(&tmW);
+    __syncwarp();
+    if (lane < NS) {
       int it = 0;
       for (int64_t b = b_first; b < nblocks; b += b_step)
         for (int kt = kt0; kt < kt1; ++kt, ++it) {
           const int s = it % NS;
+          if (s != lane) continue;
           if (!mbar_wait_bounded(smem_u32(&s_empty[s]), ((it / NS) & 1) ^ 1u, &s_abort, p.err,
                                  kKernelWaitTimeoutNs))
             break;
@@ -175,12 +181,21 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     const uint4* xv = reinterpret_cast<const uint4*>(p.x);
     if (ctid < 16) s_amax[ctid] = 0u;
     named_barrier_sync(1, cthreads);
+    // short rows (every vector of the MB rows in one batch per thread): the
+    // rows stay in registers from the max pass to the code pass, and a
+    // single token's max is reduced in the warp before the one atomic per
+    // warp (the prologue runs before any weight tile is consumed, so every
+    // round trip here delays the stream)
+    const bool one_batch = MB * nvec <= cthreads * kStageBatch;
+    uint4 vkeep[kStageBatch];
+    float wmax = 0.0f;   // this thread's max for a single token
     for (int b0 = ctid; b0 < tot; b0 += cthreads * kStageBatch) {
       uint4 v[kStageBatch];
 #pragma unroll
       for (int u = 0; u < kStageBatch; ++u) {
         const int i = b0 + u * cthreads;
         v[u] = i < tot ? xv[i] : make_uint4(0u, 0u, 0u, 0u);
+        vkeep[u] = v[u];
       }
 #pragma unroll
       for (int u = 0; u < kStageBatch; ++u) {
@@ -190,9 +205,20 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
           __half2 a2 = __habs2(h[0]);
 #pragma unroll
           for (int q = 1; q < 4; ++q) a2 = __hmax2(a2, __habs2(h[q]));
-          atomicMax(&s_amax[i / nvec], __float_as_uint(fmaxf(__low2float(a2), __high2float(a2))));
+          const float a = fmaxf(__low2float(a2), __high2float(a2));
+          if (MB == 1)
+            wmax = fmaxf(wmax, a);
+          else
+            atomicMax(&s_amax[i / nvec], __float_as_uint(a));
         }
       }
+    }
+    if (MB == 1) {
+      // after the loop, which a thread past the row's vectors never entered:
+      // every lane of every consumer warp takes part in the reduction
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+      if ((ctid & 31) == 0) atomicMax(&s_amax[0], __float_as_uint(wmax));
     }
     named_barrier_sync(1, cthreads);
     if (ctid < MB) {
@@ -207,7 +233,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 #pragma unroll
       for (int u = 0; u < kStageBatch; ++u) {
         const int i = b0 + u * cthreads;
-        v[u] = i < tot ? xv[i] : make_uint4(0u, 0u, 0u, 0u);
+        v[u] = one_batch ? vkeep[u] : (i < tot ? xv[i] : make_uint4(0u, 0u, 0u, 0u));
       }
 #pragma unroll
       for (int u = 0; u < kStageBatch; ++u) {
@@ -598,8 +624,11 @@ cudaError_t launch_one(const __half* x, const int8_t* qa, const float* sa, int64
                        int32_t* acc, const GemvSplit& sp, uint32_t* part, int num_sms,
                        cudaStream_t st) {
   auto kern = gemv_kernel<MB, INT4, PG, EPI, FUSEQ, MMA>;
-  const int NS = ring_slots(MB, sp.Ka, MMA);
-  if (NS < 4) return cudaErrorInvalidValue;
+  const int room = ring_slots(MB, sp.Ka, MMA);
+  if (room < 4) return cudaErrorInvalidValue;
+  // enough slots for every tile of a (row block, slice) when that is more
+  // than four: then all of a CTA's weight tiles are requested at once
+  const int NS = room < (sp.tps > 4 ? sp.tps : 4) ? room : (sp.tps > 4 ? sp.tps : 4);
   const size_t smem = static_cast<size_t>(NS) * kTileBytes + static_cast<size_t>(MB) * sp.Ka + 1024;
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern),
