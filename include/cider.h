@@ -256,7 +256,7 @@ cider_status_t cider_w4a8_linear_ex(const void* x, int x_dtype, int64_t M, int64
  * output tiles per CTA: the same results, possibly slower).
  *   - No cudaMalloc, cudaFree or other allocating call is made.
  *   - The first call on each device looks up the array's device address (a
- *     runtime call); make that first call before any stream capture.
+ *     runtime call that allocates nothing).
  *   - All calls share the one array and each call overwrites what it uses.
  *     Calls whose kernels may overlap on the GPU (different streams without
  *     ordering, or different host threads) race and give wrong results;

@@ -12,7 +12,8 @@
 // come from one quantization launch instead, so that each of the many CTAs
 // does not quantize the same rows again.  The producer warp issues the first
 // weight loads before that staging, so HBM streaming starts at once: weight
-// tiles of 16 rows x 256 bytes go by 2-D TMA into a ring of up to 8 slots,
+// tiles of 16 rows x 256 bytes go by 2-D TMA into a ring of as many slots
+// as a row block has tiles (at least 4, at most 12, as shared memory allows),
 // each slot refilled by its own lane of the producer warp.
 // Grids are sized to be resident in one wave; CTA c takes row blocks c,
 // c + grid, ...
