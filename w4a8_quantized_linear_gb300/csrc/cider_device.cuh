@@ -22,6 +22,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ void named_barrier_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// 16-byte shared-memory store to a 32-bit shared address.
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint32_t (&v)[4]) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+               "r"(v[3])
+               : "memory");
+}
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
@@ -212,6 +218,30 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
+}
+// Tiled shared -> global copy by the TMA engine (box of the tensor map, from
+// a box-shaped, swizzled shared-memory tile); parts of the box outside the
+// tensor are not written.  Completion is tracked by bulk async-groups of the
+// issuing thread (bulk_commit_group / bulk_wait_group*).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
+                                             int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Until at most N of this thread's bulk groups are still reading their shared-memory sources.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Until at most N of this thread's bulk groups are incomplete (writes included).
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 // As tma_load_2d, issued by either CTA of a CTA pair into its own shared
 // memory, with the completion counted on `bar` (a shared::cluster address,
@@ -415,6 +445,21 @@ __device__ __forceinline__ uint16_t y_bits(float v) {
   if constexpr (BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
   return __half_as_ushort(__float2half_rn(v));
 }
+// Two outputs at once, low | high << 16: one paired conversion instruction,
+// each value rounded to nearest even exactly as y_bits does.
+template <bool BF16>
+__device__ __forceinline__ uint32_t y_bits2(float lo, float hi) {
+  uint32_t u;
+  if constexpr (BF16) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    memcpy(&u, &h, 4);
+  } else {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    memcpy(&u, &h, 4);
+  }
+  return u;
+}
+
 
 // ---------------------------------------------------------------- exact integer -> fp16
 // Four int8 codes (byte i = code i) -> half2 {c0, c1} and {c2, c3}, exactly.

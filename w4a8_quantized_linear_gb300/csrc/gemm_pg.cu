@@ -53,8 +53,18 @@
 //   warps 8-15  epilogue, two per tensor-memory lane quarter (columns 0-127
 //               and 128-255): per group, tcgen05.ld of 32 columns at a time,
 //               fp32 running sums += s_w * acc_g; at the tile's end
-//               y = fp16(s_a * sum) with 16-byte stores.  In accumulator mode
-//               each group's exact int32 values are stored instead.
+//               y = fp16(s_a * sum) goes out by TMA: the epilogue writes the
+//               CTA's 128 x 256 outputs into the tile's last pipeline stage
+//               (64 KiB, free once the tile's last MMAs completed; the issuer
+//               leaves its "stage free" commit to the epilogue), as four
+//               [128 rows][64 columns] boxes with the 128-byte swizzle, one
+//               thread stores them with tiled TMA stores and hands the stage
+//               back once the stores have read it.  The epilogue then drains
+//               the next tile at once: storing y from registers (a warp's
+//               store touching 32 rows) had held the running sums, and with
+//               them the next tile's third group, for ~9000 cycles per tile.
+//               In accumulator mode each group's exact int32 values are
+//               stored instead.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -114,12 +124,13 @@ struct GCfg {
   static constexpr int kSwOffset = kA8Offset + kG8Slots * kG8SlotBytes;
   static constexpr int kBarOffset = kSwOffset + kGSwSlots * kGSwSlotBytes;
   // ready, empty per stage; full8, empty8 per weight slot; swf, swe per
-  // scale slot; accf, acce per accumulator; mma_done; then the
+  // scale slot; accf, acce per accumulator; mma_done; y staged; then the
   // tensor-memory slot and the abort flag
   static constexpr int kBar8 = 2 * kGStages;
   static constexpr int kBarSw = kBar8 + 2 * kG8Slots;
   static constexpr int kBarAcc = kBarSw + 2 * kGSwSlots;
-  static constexpr int kNumBars = kBarAcc + 4 + 1;
+  static constexpr int kBarY = kBarAcc + 5;
+  static constexpr int kNumBars = kBarY + 1;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -166,7 +177,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 template <bool INT4, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     gemm_pg_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                   const PgArgs p) {
+                   const __grid_constant__ CUtensorMap tmY, const PgArgs p) {
   using C = GCfg<INT4>;
   constexpr int S = kGStages;
   extern __shared__ uint8_t smem_raw[];
@@ -187,6 +198,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
   auto accf_bar = [&](int b) { return bars + 8u * (C::kBarAcc + b); };
   auto acce_bar = [&](int b) { return bars + 8u * (C::kBarAcc + 2 + b); };
   const uint32_t done_bar = bars + 8u * (C::kBarAcc + 4);
+  // a tile's y is staged in shared memory: one arrival per epilogue warp
+  const uint32_t ystg_bar = bars + 8u * C::kBarY;
   const uint32_t tmem_slot = bars + 8u * C::kNumBars;
   volatile uint32_t* abort_flag =
       reinterpret_cast<volatile uint32_t*>(gbase + C::kBarOffset + 8 * C::kNumBars + 4);
@@ -217,6 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
       mbar_init(acce_bar(b), 2 * kGEpiWarps);   // 8 epilogue warps x 2 CTAs
     }
     mbar_init(done_bar, 1);
+    mbar_init(ystg_bar, kGEpiWarps);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -304,7 +318,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
               tc_commit_pair_mc(accf_bar(b), 0x3);
             }
             if (!ok) break;
-            tc_commit_pair_mc(empty_bar(s), 0x3);
+            // a tile's last stage is handed back by the epilogue, which stages y in it
+            if (EPI == kEpiAcc || kb != p.nkb - 1) tc_commit_pair_mc(empty_bar(s), 0x3);
           }
         }
         if (!ok) *abort_flag = 1u;
@@ -430,8 +445,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
     const int row = q * 32 + lane;            // token of this thread within the CTA's 128
-    int ch = 0;
-    for (int tile = cid; tile < p.num_tiles; tile += nclusters) {
+    int ch = 0, tcount = 0;
+    for (int tile = cid; tile < p.num_tiles; tile += nclusters, ++tcount) {
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
       const int m = mt * kGTile + static_cast<int>(rank) * kGHalf + row;
       const bool mvalid = m < p.M;
@@ -500,22 +515,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
           if (lane == 0) mbar_arrive(swe_bar(js));   // this warp is done with the slot's scales
         }
       }
-      if (EPI != kEpiAcc && mvalid) {
-        const float sam = __ldg(p.sa + m);
+      if (EPI != kEpiAcc) {
+        // y of this CTA's 128 tokens x the tile's 256 columns, staged in the
+        // tile's last pipeline stage: block j (columns [64 j, 64 j + 64)) is
+        // [128 rows][128 bytes] at 16 KiB j, 16-byte chunk c of row r at chunk
+        // c ^ (r & 7) (the TMA 128-byte swizzle)
+        const int s_last = (tcount * p.nkb + p.nkb - 1) % S;
+        const uint32_t ybuf = sA(s_last);
+        const float sam = mvalid ? __ldg(p.sa + m) : 0.0f;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int n = n0 + 8 * c;
-          if (n < p.N) {   // N % 8 == 0: a group of 8 is all in or all out
-            uint32_t hw[4];
+        for (int c = 0; c < 16; ++c) {   // outputs 128 hcol + 8 c ... + 7 of the tile
+          uint32_t hw[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint32_t lo = y_bits<EPI == kEpiYb>(__fmul_rn(fsum[8 * c + 2 * i], sam));
-              const uint32_t hi = y_bits<EPI == kEpiYb>(__fmul_rn(fsum[8 * c + 2 * i + 1], sam));
-              hw[i] = lo | (hi << 16);
-            }
-            *reinterpret_cast<uint4*>(p.y + static_cast<int64_t>(m) * p.N + n) =
-                make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          for (int i = 0; i < 4; ++i)
+            hw[i] = y_bits2<EPI == kEpiYb>(__fmul_rn(fsum[8 * c + 2 * i], sam),
+                                           __fmul_rn(fsum[8 * c + 2 * i + 1], sam));
+          const int blk = 2 * hcol + (c >> 3), cc = c & 7;
+          st_shared_v4(ybuf + blk * 16384 + row * 128 + ((cc ^ (row & 7)) << 4), hw);
+        }
+        fence_proxy_async_smem();   // the TMA engine reads what these threads wrote
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ystg_bar);
+        // the first epilogue warp waits for all eight warps' parts and one of
+        // its threads stores them; the other warps go on to the next tile
+        if (e == 0) {
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(ystg_bar, tcount & 1, abort_flag, err,
+                                                          kGWaitNs)))
+            goto done;
+          if (lane == 0) {
+            const int m0 = mt * kGTile + static_cast<int>(rank) * kGHalf;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tma_store_2d(&tmY, ybuf + j * 16384, nt * kGTile + 64 * j, m0);
+            bulk_commit_group();
+            bulk_wait_group_read<0>();   // the stage may be refilled once the stores have read it
+            mbar_arrive(empty_bar(s_last));
           }
+          __syncwarp();
         }
       }
     }
@@ -523,6 +559,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
 done:
   __syncwarp();
   cp_async_wait<0>();   // also after an abort: no copy into shared memory outlives the CTA
+  if (EPI != kEpiAcc && warp == kGEpiWarp0 && lane == 0) bulk_wait_group<0>();   // y stores written
   if (warp == kGMmaWarp) {
     // the even CTA's last commit reaches both CTAs; wait for it (bounded, and
     // also after an abort) so no MMA is in flight when the pair frees its
@@ -578,8 +615,8 @@ cudaError_t pg_max_clusters(int* out) {
 }
 
 template <bool INT4, int EPI>
-cudaError_t launch_pg(const CUtensorMap& tmX, const CUtensorMap& tmW, const PgArgs& a, int clusters,
-                      cudaStream_t st) {
+cudaError_t launch_pg(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap& tmY,
+                      const PgArgs& a, int clusters, cudaStream_t st) {
   using C = GCfg<INT4>;
   auto kern = gemm_pg_kernel<INT4, EPI>;
   static std::atomic<uint64_t> attr_done{0};
@@ -597,7 +634,7 @@ cudaError_t launch_pg(const CUtensorMap& tmX, const CUtensorMap& tmW, const PgAr
     regs_ok.store(fa.numRegs * kGThreads >= kGRegsNeeded ? 1 : -1, std::memory_order_relaxed);
   }
   if (regs_ok.load(std::memory_order_relaxed) < 0) return cudaErrorInvalidConfiguration;
-  kern<<<2 * clusters, kGThreads, C::kSmemBytes, st>>>(tmX, tmW, a);
+  kern<<<2 * clusters, kGThreads, C::kSmemBytes, st>>>(tmX, tmW, tmY, a);
   return cudaGetLastError();
 }
 
@@ -615,6 +652,14 @@ cudaError_t launch_gemm_pg(const __half* qa16, const float* sa, int64_t M, int64
   if (!make_tensor_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, wbytes, N, wbytes,
                           int4 ? kGSubK / 2 : kGSubK, kGHalf,
                           int4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  // y [M, N] of 2-byte outputs (fp16 or bf16 bits), stored in [128 rows][64 columns] boxes; in
+  // accumulator mode the map is not used (a valid one over the weights is passed instead)
+  CUtensorMap tmY;
+  if (mode != kEpiAcc ? !make_tensor_map_2d(&tmY, CU_TENSOR_MAP_DATA_TYPE_UINT16, y, N, M, N * 2, 64,
+                                            kGHalf, CU_TENSOR_MAP_SWIZZLE_128B)
+                      : !make_tensor_map_2d(&tmY, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, wbytes, N, wbytes,
+                                            16, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   int nc = 0;
   cudaError_t e = pg_max_clusters(&nc);
@@ -636,12 +681,12 @@ cudaError_t launch_gemm_pg(const __half* qa16, const float* sa, int64_t M, int64
   if (e != cudaSuccess) return e;
   const int clusters = a.num_tiles < nc ? a.num_tiles : nc;
   if (int4)
-    return mode == kEpiY    ? launch_pg<true, kEpiY>(tmX, tmW, a, clusters, st)
-           : mode == kEpiYb ? launch_pg<true, kEpiYb>(tmX, tmW, a, clusters, st)
-                            : launch_pg<true, kEpiAcc>(tmX, tmW, a, clusters, st);
-  return mode == kEpiY    ? launch_pg<false, kEpiY>(tmX, tmW, a, clusters, st)
-         : mode == kEpiYb ? launch_pg<false, kEpiYb>(tmX, tmW, a, clusters, st)
-                          : launch_pg<false, kEpiAcc>(tmX, tmW, a, clusters, st);
+    return mode == kEpiY    ? launch_pg<true, kEpiY>(tmX, tmW, tmY, a, clusters, st)
+           : mode == kEpiYb ? launch_pg<true, kEpiYb>(tmX, tmW, tmY, a, clusters, st)
+                            : launch_pg<true, kEpiAcc>(tmX, tmW, tmY, a, clusters, st);
+  return mode == kEpiY    ? launch_pg<false, kEpiY>(tmX, tmW, tmY, a, clusters, st)
+         : mode == kEpiYb ? launch_pg<false, kEpiYb>(tmX, tmW, tmY, a, clusters, st)
+                          : launch_pg<false, kEpiAcc>(tmX, tmW, tmY, a, clusters, st);
 }
 
 }  // namespace cider
