@@ -28,16 +28,23 @@
 //               [128 m][64 k] sub-tiles per 128-K stage) into the 3-stage
 //               operand ring; the copies of both CTAs complete on the even
 //               CTA's "ready" barrier.
-//   warp 1      even CTA only, one thread: waits until both CTAs' stages are
-//               ready, issues 8 MMAs (K = 16 each) into one of two 256-column
-//               accumulators and commits to both CTAs' barriers (stage free;
-//               accumulator full).  Both CTAs' warp 1 allocate tensor memory.
-//               128-K stages halve the per-stage synchronisation cost, which
-//               with 64-K stages kept the tensor pipe ~30 % idle.
+//   warps 1, 15 the two MMA issuers, even CTA only, one thread each, taking
+//               alternate stages: wait until both CTAs' stage is ready, issue
+//               8 MMAs (K = 16 each) into one of two 256-column accumulators
+//               and commit to both CTAs' barriers (stage free; accumulator
+//               full).  A token passed between them keeps the MMAs in stage
+//               order.  One thread alone needed ~1300 cycles per stage for its
+//               chain of waits, fences, commits and MMA issues (~75 cycles
+//               each), more than the stage's 1024 cycles of MMAs.  Both CTAs'
+//               warp 1 allocate tensor memory.  128-K stages halve the
+//               per-stage synchronisation cost, which with 64-K stages kept
+//               the tensor pipe ~30 % idle.
 //   warps 10-13 epilogue, one per tensor-memory lane quarter: drain the
 //               accumulator (tcgen05.ld: a thread holds 32 consecutive weight
-//               rows of its token), dequantize, store fp16 y with 16-byte
-//               stores (or int32 accumulators), release the accumulator.
+//               rows of its token), release it once the last columns are in
+//               registers, dequantize, store fp16 y (32-byte stores when rows
+//               start 32-byte aligned, else 16-byte ones; a warp's store
+//               touches 32 rows) or int32 accumulators.
 //   converters  two groups of 4 warps (warps 2-9) taking alternate stages:
 //               each thread converts its weight row's 128 codes of the stage
 //               (two 64-K sub-tiles) and writes them in the canonical K-major
@@ -102,7 +109,8 @@ constexpr int kPStages = 3;
 constexpr int kPConvWarp0 = 2;                   // two groups of 4 converter warps
 constexpr int kPEpiWarp0 = 10;
 constexpr int kPW8Warp = 14;
-constexpr int kPThreads = 32 * (kPW8Warp + 1);
+constexpr int kPMma2Warp = 15;                   // the second MMA issuer
+constexpr int kPThreads = 32 * (kPMma2Warp + 1);
 // the even CTA's producer arrival (with both CTAs' activation bytes) + 4
 // converter warps x 2 CTAs
 constexpr int kPReadyCount = 9;
@@ -118,7 +126,8 @@ struct PCfg {
   // mma_done; then the tensor-memory slot and the abort flag
   static constexpr int kBar8 = 2 * kPStages;
   static constexpr int kBar2 = kBar8 + 2 * kP8Slots;
-  static constexpr int kNumBars = kBar2 + 5;
+  static constexpr int kBarTok = kBar2 + 5;       // the issuers' turn tokens
+  static constexpr int kNumBars = kBarTok + 2;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -194,13 +203,29 @@ __device__ __forceinline__ void store8_y(const PairArgs& p, int m, float sam, in
                                          const float (&w)[8]) {
   uint32_t h[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t lo = y_bits<BF16>(__fmul_rn(__fmul_rn(f[2 * i], sam), w[2 * i]));
-    const uint32_t hi = y_bits<BF16>(__fmul_rn(__fmul_rn(f[2 * i + 1], sam), w[2 * i + 1]));
-    h[i] = lo | (hi << 16);
-  }
+  for (int i = 0; i < 4; ++i)
+    h[i] = y_bits2<BF16>(__fmul_rn(__fmul_rn(f[2 * i], sam), w[2 * i]),
+                         __fmul_rn(__fmul_rn(f[2 * i + 1], sam), w[2 * i + 1]));
   *reinterpret_cast<uint4*>(p.y + static_cast<int64_t>(m) * p.N + n0) =
       make_uint4(h[0], h[1], h[2], h[3]);
+}
+
+// The same for sixteen outputs n0 .. n0 + 15 with one 32-byte store (the
+// address must be 32-byte aligned).  A lane's stores go to its own token's
+// row, so a warp's store touches 32 rows: wider stores halve the requests.
+template <bool BF16>
+__device__ __forceinline__ void store16_y(const PairArgs& p, int m, float sam, int n0,
+                                          const float (&f)[16], const float (&w)[16]) {
+  uint32_t h[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    h[i] = y_bits2<BF16>(__fmul_rn(__fmul_rn(f[2 * i], sam), w[2 * i]),
+                         __fmul_rn(__fmul_rn(f[2 * i + 1], sam), w[2 * i + 1]));
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(
+                   p.y + static_cast<int64_t>(m) * p.N + n0),
+               "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]), "r"(h[4]), "r"(h[5]), "r"(h[6]),
+               "r"(h[7])
+               : "memory");
 }
 
 template <bool INT4, int EPI>
@@ -224,6 +249,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   auto accf_bar = [&](int b) { return bars + 8u * (C::kBar2 + b); };
   auto acce_bar = [&](int b) { return bars + 8u * (C::kBar2 + 2 + b); };
   const uint32_t done_bar = bars + 8u * (C::kBar2 + 4);
+  // turn token of issuer b: completes once per stage the other issuer has issued
+  auto tok_bar = [&](int b) { return bars + 8u * (C::kBarTok + b); };
   const uint32_t tmem_slot = bars + 8u * C::kNumBars;
   volatile uint32_t* abort_flag =
       reinterpret_cast<volatile uint32_t*>(gbase + C::kBarOffset + 8 * C::kNumBars + 4);
@@ -245,10 +272,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       mbar_init(empty8_bar(j), 4);     // the 4 warps of the converter group of this use
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(accf_bar(b), 1);
+      mbar_init(accf_bar(b), 2);       // both issuers, each after its own MMAs of the chunk
       mbar_init(acce_bar(b), 8);       // 4 epilogue warps x 2 CTAs
     }
-    mbar_init(done_bar, 1);
+    mbar_init(done_bar, 2);
+    mbar_init(tok_bar(0), 1);
+    mbar_init(tok_bar(1), 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -293,8 +322,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       __syncwarp();
       if (*abort_flag) break;
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (even CTA)
+  } else if (warp == 1 || warp == kPMma2Warp) {
+    // ------------------------------------------------------------ MMA issuers (even CTA)
+    // Issuer me (warp 1: 0, warp 15: 1) issues the stages with it % 2 == me.
+    // A lone issuer needed ~1300 cycles per stage for its chain of barrier
+    // waits, fences, commits and eight MMA issues (~75 cycles each), against
+    // 1024 cycles of tensor-core work; two issuers overlap their chains.  The
+    // MMAs still reach the tensor core in stage order: before issuing stage
+    // it an issuer waits for its token, which the other issuer gives once it
+    // has issued stage it - 1.  Both issuers pass every stage's "ready"
+    // barrier in order (so no parity wait can be satisfied by an older phase)
+    // and both commit "accumulator full" at the end of every chunk, each
+    // after its own MMAs of the chunk (the barrier counts two arrivals).
+    const int me = warp == 1 ? 0 : 1;
     if (rank == 0) {
       constexpr uint32_t idesc_fast = idesc_f16_f32(kPTileM, kPTileN);
       constexpr uint32_t idesc_slow = idesc_f16_f32(kPTileM, kPTileN / kPSlowPasses);
@@ -314,30 +354,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
               const bool cend =
                   fast ? (kb == kb1 - 1) : ((kr % kPChunkKB) == kPChunkKB - 1 || kb == kb1 - 1);
               const int b = ch & 1;
-              if (cstart && ch >= 2) {
-                // accumulator b was last used by chunk ch - 2: wait until both CTAs drained it
-                ok = mbar_wait_bounded(acce_bar(b), ((ch - 2) >> 1) & 1, abort_flag, err, kPWaitNs);
-                if (!ok) break;
-                tc_fence_after();
-              }
               const int s = it % S;
               const uint32_t ph = (it / S) & 1;
               if (!mbar_wait_bounded(ready_bar(s), ph, abort_flag, err, kPWaitNs)) {
                 ok = false;
                 break;
               }
-              tc_fence_after();
-              const uint64_t adesc = smem_desc_k_sw128(sA(s));
-              // slow pass p uses weight rows [32 p, 32 p + 32) of each CTA's 128
-              const uint64_t bdesc = smem_desc_k_sw128(sB(s) + (fast ? 0 : pass * (32 * 128)));
+              if ((it & 1) == me) {
+                // accumulator b was last used by chunk ch - 2: wait until both CTAs drained it
+                if (cstart && ch >= 2 &&
+                    !mbar_wait_bounded(acce_bar(b), ((ch - 2) >> 1) & 1, abort_flag, err, kPWaitNs)) {
+                  ok = false;
+                  break;
+                }
+                // stage it - 1 is the other issuer's ((it - 1) >> 1)-th
+                if (it >= 1 &&
+                    !mbar_wait_bounded(tok_bar(me), ((it - 1) >> 1) & 1, abort_flag, err, kPWaitNs)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                const uint64_t adesc = smem_desc_k_sw128(sA(s));
+                // slow pass p uses weight rows [32 p, 32 p + 32) of each CTA's 128
+                const uint64_t bdesc = smem_desc_k_sw128(sB(s) + (fast ? 0 : pass * (32 * 128)));
 #pragma unroll
-              for (int j = 0; j < kPBK / kPUmmaK; ++j) {
-                // sub-tile j / 4, K step j % 4 (+32 bytes each) inside it
-                const uint64_t off = static_cast<uint64_t>((j >> 2) * (kPSubBytes >> 4) + (j & 3) * 2);
-                tc_mma_ss_pair(tmem + b * kPAccCols, adesc + off, bdesc + off,
-                               fast ? idesc_fast : idesc_slow, (cstart && j == 0) ? 0u : 1u);
+                for (int j = 0; j < kPBK / kPUmmaK; ++j) {
+                  // sub-tile j / 4, K step j % 4 (+32 bytes each) inside it
+                  const uint64_t off =
+                      static_cast<uint64_t>((j >> 2) * (kPSubBytes >> 4) + (j & 3) * 2);
+                  tc_mma_ss_pair(tmem + b * kPAccCols, adesc + off, bdesc + off,
+                                 fast ? idesc_fast : idesc_slow, (cstart && j == 0) ? 0u : 1u);
+                }
+                mbar_arrive(tok_bar(me ^ 1));   // the other issuer may issue stage it + 1
+                tc_commit_pair_mc(empty_bar(s), 0x3);
               }
-              tc_commit_pair_mc(empty_bar(s), 0x3);
               if (cend) {
                 tc_commit_pair_mc(accf_bar(b), 0x3);
                 ++ch;
@@ -455,6 +505,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // tensor-memory lane quarter of this warp
+    // y rows start 32-byte aligned: sixteen outputs per store
+    const bool y_wide = (reinterpret_cast<uintptr_t>(p.y) % 32 == 0) && (p.N % 16 == 0);
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
     int ch = 0;
@@ -526,22 +578,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           goto done;
         tc_fence_after();
         // column j of the accumulator is weight row nt * 256 + j
+        const bool wide = !piece && EPI != kEpiAcc && y_wide;
 #pragma unroll 1
         for (int c8 = 0; c8 < kPAccCols / 32; ++c8) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + b * kPAccCols + c8 * 32, v);
           tmem_wait_ld();
+          if (c8 == kPAccCols / 32 - 1) {
+            // the last columns are in registers: the accumulator is free for the next tile but one
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(acce_leader0 + 8u * b);
+          }
+          if (wide) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            int iv[8];
+            for (int g = 0; g < 2; ++g) {
+              const int col = c8 * 32 + g * 16;
+              float f[16], w[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) iv[i] = __float2int_rn(__uint_as_float(v[g * 8 + i]));
-            emit8(c8 * 32 + g * 8, iv);
+              for (int i = 0; i < 16; ++i)
+                f[i] = __int2float_rn(__float2int_rn(__uint_as_float(v[g * 16 + i])));
+#pragma unroll
+              for (int i = 0; i < 16; ++i) w[i] = __shfl_sync(0xffffffffu, swr[i & 7], (col >> 3) + (i >> 3));
+              // N % 16 == 0 here: a group of 16 is all in or all out
+              if (mvalid && n_tile + col < p.N) store16_y<EPI == kEpiYb>(p, m, sam, n_tile + col, f, w);
+            }
+          } else {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              int iv[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) iv[i] = __float2int_rn(__uint_as_float(v[g * 8 + i]));
+              emit8(c8 * 32 + g * 8, iv);
+            }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(acce_leader0 + 8u * b);
         ++ch;
       } else {
         for (int pass = 0; pass < kPSlowPasses; ++pass) {
