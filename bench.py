@@ -300,6 +300,17 @@ def host_cpu() -> dict:
     except OSError:
         pass
     if model is None:
+        # Arm hosts list no model name in /proc/cpuinfo; lscpu decodes the part number
+        try:
+            import subprocess
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.lower().startswith("model name:"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    if model is None:
         import platform
         model = platform.processor() or platform.machine()
     return {"nproc": os.cpu_count(), "cpu_model": model}
