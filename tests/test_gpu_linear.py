@@ -398,3 +398,34 @@ def test_trim_scratch_pool_keeps_results(cider):
     cider.cider_trim_scratch_pool(1 << 20)
     assert_bits_equal(to_host(y1), to_host(y0), "after trimming the pool")
     assert cider.cider_check_device_error() == 0
+
+
+@pytest.mark.parametrize("gs,bits", [(0, 8), (0, 4), (128, 8), (64, 4)])
+@pytest.mark.parametrize("y_dtype", ["f16", "bf16"])
+def test_output_views_at_16_byte_offsets(cider, gs, bits, y_dtype):
+    """y written into a view that starts 16 bytes (not 32) into its buffer,
+    with N % 16 == 0: the per-channel epilogue then takes its 16-byte-store
+    path and the per-group kernel's TMA stores start at a 16-byte boundary.
+    The outputs equal the oracle's (per channel bit for bit, per group within
+    the tolerance); the bytes around the view stay untouched."""
+    M, N, K = 300, 1024, 1024
+    x = inputs.activations(M, K, seed=21)
+    qw_dev, qv, sw = make_weights(N, K, gs, bits, seed=22)
+    dt = torch.float16 if y_dtype == "f16" else torch.bfloat16
+    big = torch.full((M * N + 16,), 7.0, dtype=dt, device="cuda")
+    y = big[8:8 + M * N].view(M, N)
+    assert y.data_ptr() % 32 == 16
+    fn = cider.cider_w8a8_linear_ex if bits == 8 else cider.cider_w4a8_linear_ex
+    fn(to_dev(x), to_dev(qw_dev), to_dev(sw), gs, y_dtype=dt, out=y)
+    ref = oracle.linear(x, qv, sw, gs, out_bf16=(y_dtype == "bf16"))
+    got = y.cpu().view(torch.int16).numpy().view(np.uint16) if y_dtype == "bf16" else to_host(y)
+    want = ref.view(np.uint16) if y_dtype == "bf16" else ref
+    if gs == 0:
+        assert_bits_equal(got, want, f"16-byte offset view, bits {bits}, {y_dtype}")
+    elif y_dtype == "f16":
+        assert_fp16_close(got, want, f"16-byte offset view, bits {bits} gs {gs}")
+    else:
+        from tests.test_gpu_bf16 import assert_bf16_close
+        assert_bf16_close(got, want, f"16-byte offset view, bits {bits} gs {gs}")
+    edge = big.cpu().float().numpy()
+    assert np.all(edge[:8] == 7.0) and np.all(edge[8 + M * N:] == 7.0)
