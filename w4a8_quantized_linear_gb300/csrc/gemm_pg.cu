@@ -174,7 +174,10 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 
-template <bool INT4, int EPI>
+// BATCH: the converters load a sub-tile's code chunks before converting them
+// (their load latencies overlap); measured faster at gs 128 and slower at gs 64
+// (where the two drains per stage pace the kernel), so it is chosen by group size.
+template <bool INT4, int EPI, bool BATCH>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     gemm_pg_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmY, const PgArgs p) {
@@ -397,10 +400,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
           if (!INT4) {
             // 64-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3);
             // its 16 codes become fp16 chunks 2c and 2c + 1 of the 128-byte row
+            uint4 vin[4];
+            if (BATCH) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                vin[c] = *reinterpret_cast<const uint4*>(arow + row * 64 +
+                                                         ((c ^ ((row >> 1) & 3)) << 4));
+            }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-              const uint4 v = *reinterpret_cast<const uint4*>(
-                  arow + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
+              const uint4 v = BATCH ? vin[c]
+                                    : *reinterpret_cast<const uint4*>(
+                                          arow + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
               uint32_t h[8];
               s8x4_to_h2x2(v.x, h[0], h[1]);
               s8x4_to_h2x2(v.y, h[2], h[3]);
@@ -414,10 +425,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
           } else {
             // 32-byte swizzle: chunk c of row r sits at chunk c ^ ((r >> 2) & 1); its 32
             // codes become fp16 chunks 4c .. 4c + 3
+            uint4 vin[2];
+            if (BATCH) {
+#pragma unroll
+              for (int c = 0; c < 2; ++c)
+                vin[c] = *reinterpret_cast<const uint4*>(arow + row * 32 +
+                                                         ((c ^ ((row >> 2) & 1)) << 4));
+            }
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-              const uint4 v = *reinterpret_cast<const uint4*>(
-                  arow + row * 32 + ((c ^ ((row >> 2) & 1)) << 4));
+              const uint4 v = BATCH ? vin[c]
+                                    : *reinterpret_cast<const uint4*>(
+                                          arow + row * 32 + ((c ^ ((row >> 2) & 1)) << 4));
               const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
               for (int q4 = 0; q4 < 4; ++q4) {
@@ -588,7 +607,7 @@ cudaError_t pg_max_clusters(int* out) {
   if (e != cudaSuccess) return e;
   int nc = dev < 64 ? cached[dev].load(std::memory_order_relaxed) : 0;
   if (nc <= 0) {
-    auto kern = gemm_pg_kernel<false, kEpiY>;
+    auto kern = gemm_pg_kernel<false, kEpiY, true>;
     static std::atomic<uint64_t> attr_done{0};
     e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), GCfg<false>::kSmemBytes,
                                 attr_done);
@@ -614,11 +633,11 @@ cudaError_t pg_max_clusters(int* out) {
   return cudaSuccess;
 }
 
-template <bool INT4, int EPI>
+template <bool INT4, int EPI, bool BATCH>
 cudaError_t launch_pg(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap& tmY,
                       const PgArgs& a, int clusters, cudaStream_t st) {
   using C = GCfg<INT4>;
-  auto kern = gemm_pg_kernel<INT4, EPI>;
+  auto kern = gemm_pg_kernel<INT4, EPI, BATCH>;
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::kSmemBytes,
                                           attr_done);
@@ -680,13 +699,17 @@ cudaError_t launch_gemm_pg(const __half* qa16, const float* sa, int64_t M, int64
   e = device_error_word(&a.err);
   if (e != cudaSuccess) return e;
   const int clusters = a.num_tiles < nc ? a.num_tiles : nc;
-  if (int4)
-    return mode == kEpiY    ? launch_pg<true, kEpiY>(tmX, tmW, tmY, a, clusters, st)
-           : mode == kEpiYb ? launch_pg<true, kEpiYb>(tmX, tmW, tmY, a, clusters, st)
-                            : launch_pg<true, kEpiAcc>(tmX, tmW, tmY, a, clusters, st);
-  return mode == kEpiY    ? launch_pg<false, kEpiY>(tmX, tmW, tmY, a, clusters, st)
-         : mode == kEpiYb ? launch_pg<false, kEpiYb>(tmX, tmW, tmY, a, clusters, st)
-                          : launch_pg<false, kEpiAcc>(tmX, tmW, tmY, a, clusters, st);
+#define CIDER_PG_LAUNCH(I4, B)                                                               \
+  return mode == kEpiY    ? launch_pg<I4, kEpiY, B>(tmX, tmW, tmY, a, clusters, st)          \
+         : mode == kEpiYb ? launch_pg<I4, kEpiYb, B>(tmX, tmW, tmY, a, clusters, st)         \
+                          : launch_pg<I4, kEpiAcc, B>(tmX, tmW, tmY, a, clusters, st);
+  if (int4) {
+    if (group_size == 128) CIDER_PG_LAUNCH(true, true)
+    CIDER_PG_LAUNCH(true, false)
+  }
+  if (group_size == 128) CIDER_PG_LAUNCH(false, true)
+  CIDER_PG_LAUNCH(false, false)
+#undef CIDER_PG_LAUNCH
 }
 
 }  // namespace cider
