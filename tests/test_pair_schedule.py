@@ -71,6 +71,7 @@ def check_schedule(M, N, K, pairs):
         s = info["pieces"]
         assert info["whole_tiles"] % pairs == 0 and info["cut_tiles"] == tiles % pairs
         assert info["cut_tiles"] * s <= pairs and s * 4 <= nkb
+        assert s <= 16, "the pieces' slices of the partials must fit the pipeline stages"
         rounds = tiles // pairs
         assert rounds * nkb + -(-nkb // s) < (rounds + 1) * nkb
         lens = [u[2] - u[1] for us in by_pair.values() for u in us if u[3] == PIECE]
@@ -83,7 +84,8 @@ def check_schedule(M, N, K, pairs):
 SHAPES = [(128, 2560, 2560), (4096, 10240, 2560), (3455, 6144, 2048), (1024, 10240, 2560),
           (4096, 2560, 10240), (8192, 10240, 2560), (128, 10240, 2560), (1334, 2048, 2048),
           (700, 264, 2560), (700, 264, 10240), (257, 384, 4096), (40, 264, 6144), (17, 136, 128),
-          (300, 200, 2048), (4096, 12288, 4096), (2393, 6144, 2048), (1, 8, 128)]
+          (300, 200, 2048), (4096, 12288, 4096), (2393, 6144, 2048), (1, 8, 128),
+          (256, 256, 10240)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)

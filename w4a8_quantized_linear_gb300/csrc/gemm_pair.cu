@@ -123,11 +123,13 @@ struct PCfg {
   static constexpr int kA8Offset = kPStages * kPStageBytes;
   static constexpr int kBarOffset = kA8Offset + kP8Slots * 8192;
   // ready, empty per stage; full8, empty8 per weight slot; accf x2, acce x2,
-  // mma_done; then the tensor-memory slot and the abort flag
+  // mma_done; the issuers' turn tokens; the pieces' partials copied in; then
+  // the tensor-memory slot and the abort flag
   static constexpr int kBar8 = 2 * kPStages;
   static constexpr int kBar2 = kBar8 + 2 * kP8Slots;
   static constexpr int kBarTok = kBar2 + 5;       // the issuers' turn tokens
-  static constexpr int kNumBars = kBarTok + 2;
+  static constexpr int kBarRed = kBarTok + 2;     // a cut tile's partials are in shared memory
+  static constexpr int kNumBars = kBarRed + 1;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -251,6 +253,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   const uint32_t done_bar = bars + 8u * (C::kBar2 + 4);
   // turn token of issuer b: completes once per stage the other issuer has issued
   auto tok_bar = [&](int b) { return bars + 8u * (C::kBarTok + b); };
+  const uint32_t red_bar = bars + 8u * C::kBarRed;
   const uint32_t tmem_slot = bars + 8u * C::kNumBars;
   volatile uint32_t* abort_flag =
       reinterpret_cast<volatile uint32_t*>(gbase + C::kBarOffset + 8 * C::kNumBars + 4);
@@ -278,6 +281,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     mbar_init(done_bar, 2);
     mbar_init(tok_bar(0), 1);
     mbar_init(tok_bar(1), 1);
+    mbar_init(red_bar, 4);   // one arrival per epilogue warp
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -648,59 +652,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         }
       }
       if (piece) {
-        // every lane counts its own stores of the partial; the other pieces'
-        // warps of the same CTA rank and lane quarter wait for all 32
+        // every lane counts its own stores of the partial
         gpu_count_release(p.flags + (cid * 2 + rank) * 4 + q);
         const int s = p.sk_split, k = cid % s, c0 = cid - k;
-        for (int kk = 0; kk < s; ++kk)
-          if (kk != k && !__all_sync(0xffffffffu, gpu_count_wait_bounded(
-                                                      p.flags + ((c0 + kk) * 2 + rank) * 4 + q, 32,
-                                                      abort_flag, err, kPWaitNs)))
-            goto done;
         int j0, j1;
         piece_slice(k, s, &j0, &j1);
-        // up to 8 column groups (32 weight rows) at a time, two pieces' loads
-        // in flight; the slots have room for every token row of the tile, so
-        // all lanes load (rows past M are summed but not stored)
+        // The slice [j0, j1) of every piece's partial (all 128 tokens) is
+        // contiguous, (j1 - j0) x 2 KiB; the pipeline stages are free now (a
+        // cut tile is a pair's last unit and its MMAs have completed), so the
+        // s slices are copied there by bulk copies and summed from shared
+        // memory: reading them from L2 one dependent round trip after another
+        // was the slowest part of a cut tile.  Epilogue warp e copies pieces
+        // e, e + 4, ... once all four lane quarters of each have stored.
+        const int e = warp - kPEpiWarp0;
+        const uint32_t slice_bytes = static_cast<uint32_t>(j1 - j0) * kPHalf * 16;
+        const uint32_t sbuf = sA(0);
+        for (int kk = e; kk < s; kk += 4)
+          for (int qq = 0; qq < 4; ++qq)
+            if (!__all_sync(0xffffffffu, gpu_count_wait_bounded(
+                                             p.flags + ((c0 + kk) * 2 + rank) * 4 + qq, 32,
+                                             abort_flag, err, kPWaitNs)))
+              goto done;
+        if (lane == 0) {
+          // the partials (other SMs' stores, acquired above) are read by the TMA engine
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          uint32_t bytes = 0;
+          for (int kk = e; kk < s; kk += 4) bytes += slice_bytes;
+          mbar_arrive_expect_tx(red_bar, bytes);
+          for (int kk = e; kk < s; kk += 4)
+            bulk_load(sbuf + kk * slice_bytes,
+                      p.part + (static_cast<int64_t>(c0 + kk) * 2 + rank) * (kPTileN / 4) * kPHalf +
+                          static_cast<int64_t>(j0) * kPHalf,
+                      slice_bytes, red_bar);
+        }
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(red_bar, 0, abort_flag, err, kPWaitNs)))
+          goto done;
+        const int4* sl = reinterpret_cast<const int4*>(gbase + (sbuf - base)) + row;
+        // two column groups (8 weight rows) at a time
 #pragma unroll 1
-        for (int jb = j0; jb < j1; jb += 8) {
-          const int nj = j1 - jb;
-          int sum[32];
+        for (int jb = j0; jb < j1; jb += 2) {
+          int iv[8];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) sum[i] = 0;
-#pragma unroll 1
-          for (int kk = 0; kk < s; kk += 2) {
-            const int4* src0 = slot(c0 + kk) + jb * kPHalf;
-            const int4* src1 = slot(c0 + (kk + 1 < s ? kk + 1 : kk)) + jb * kPHalf;
-            const bool two = kk + 1 < s;
-            int4 t0[8], t1[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int ii = i < nj ? i : 0;   // past the slice: reload group 0, unused
-              t0[i] = __ldcg(src0 + ii * kPHalf);
-              t1[i] = __ldcg(src1 + ii * kPHalf);
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              if (!two) t1[i] = make_int4(0, 0, 0, 0);
-              sum[4 * i + 0] += t0[i].x + t1[i].x;
-              sum[4 * i + 1] += t0[i].y + t1[i].y;
-              sum[4 * i + 2] += t0[i].z + t1[i].z;
-              sum[4 * i + 3] += t0[i].w + t1[i].w;
-            }
+          for (int i = 0; i < 8; ++i) iv[i] = 0;
+#pragma unroll 4
+          for (int kk = 0; kk < s; ++kk) {
+            const int4* src = sl + (kk * (j1 - j0) + (jb - j0)) * kPHalf;
+            const int4 a = src[0], b = src[kPHalf];
+            iv[0] += a.x; iv[1] += a.y; iv[2] += a.z; iv[3] += a.w;
+            iv[4] += b.x; iv[5] += b.y; iv[6] += b.z; iv[7] += b.w;
           }
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            if (2 * g < nj) {   // warp-uniform
-              const int col = (jb + 2 * g) * 4;
-              float w[8];
-              if (EPI != kEpiAcc) scales8(col, w);
-              int iv[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) iv[i] = sum[8 * g + i];
-              if (mvalid && n_tile + col < p.N) store8(n_tile + col, iv, w);
-            }
-          }
+          const int col = jb * 4;
+          float w[8];
+          if (EPI != kEpiAcc) scales8(col, w);
+          if (mvalid && n_tile + col < p.N) store8(n_tile + col, iv, w);
         }
       }
     }
@@ -767,6 +772,7 @@ cudaError_t pair_max_clusters(int* out) {
 // it pays only when it saves many blocks (long K: 4096 x 2560 x 10240 went
 // from 160 to 128 us; 4096 x 10240 x 2560, halves of 10 blocks, lost 2 %).
 constexpr int kSkMinBlocks = 4;        // shortest piece worth giving a pair, in 128-K blocks
+constexpr int kSkMaxSplit = 16;        // pieces per cut tile: their slices of the partials fit the stages
 constexpr int kSkFixupBlocks = 2;      // storing, waiting for and adding partials, in blocks
 constexpr int kSkAfterRoundsBlocks = 24;   // extra cost of cutting after whole rounds
 
@@ -795,6 +801,7 @@ PairPlan pair_plan(int64_t M, int64_t N, int64_t K, int nc, bool allow_sk) {
   if (rem == 0) return pl;
   int split = nc / rem;
   if (split > pl.nkb / kSkMinBlocks) split = pl.nkb / kSkMinBlocks;
+  if (split > kSkMaxSplit) split = kSkMaxSplit;
   if (split < 2) return pl;
   const int64_t cost_whole = static_cast<int64_t>(rounds + 1) * pl.nkb;
   const int64_t cost_sk = static_cast<int64_t>(rounds) * pl.nkb + (pl.nkb + split - 1) / split +
