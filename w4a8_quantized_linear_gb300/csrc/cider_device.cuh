@@ -497,6 +497,30 @@ __device__ __forceinline__ void s4x8_to_h2x4(uint32_t w, uint32_t (&h)[4]) {
   }
 }
 
+// The same eight codes as fp16 pairs of even and of odd codes:
+// even = {c0, c2} {c4, c6}, odd = {c1, c3} {c5, c7} (the order in which
+// offset_nibbles_to_s8x4 of the low / high nibbles followed by s8x4_to_h2x2
+// gives them), in one step: bytes (0, 1) and (2, 3) go to the two halves,
+// the low nibbles into the mantissa of 1024 (1024 + t, minus 1032) and the
+// high nibbles four bits up (1024 + 16 t, times 1/16 minus 72).  All exact.
+__device__ __forceinline__ void s4x8_to_h2_eo(uint32_t w, uint32_t (&ev)[2], uint32_t (&od)[2]) {
+  const uint32_t u = w ^ 0x88888888u;
+  const __half2 one = __halves2half2(__ushort_as_half(0x3C00u), __ushort_as_half(0x3C00u));
+  const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2C00u), __ushort_as_half(0x2C00u));
+  const __half2 bias_lo = __halves2half2(__ushort_as_half(0xE408u), __ushort_as_half(0xE408u));
+  const __half2 bias_hi = __halves2half2(__ushort_as_half(0xD480u), __ushort_as_half(0xD480u));
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const uint32_t b = __byte_perm(u, 0u, p == 0 ? 0x4140u : 0x4342u);   // [byte 2p, 0, byte 2p+1, 0]
+    uint32_t lo = (b & 0x000F000Fu) | 0x64006400u;
+    uint32_t hi = (b & 0x00F000F0u) | 0x64006400u;
+    const __half2 rl = __hfma2(*reinterpret_cast<__half2*>(&lo), one, bias_lo);
+    const __half2 rh = __hfma2(*reinterpret_cast<__half2*>(&hi), sixteenth, bias_hi);
+    ev[p] = *reinterpret_cast<const uint32_t*>(&rl);
+    od[p] = *reinterpret_cast<const uint32_t*>(&rh);
+  }
+}
+
 // x / s correctly rounded (IEEE binary32, round to nearest even), from
 // r = RN(1/s) and two FMAs: q0 = RN(x r) is within one ulp of x / s, the
 // residual x - s q0 is exact in one FMA, and RN(q0 + residual * r) is the

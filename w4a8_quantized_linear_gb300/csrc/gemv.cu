@@ -313,13 +313,19 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
               iacc[4 + i] += __float2int_rn(c1[i]);
             }
           } else {
+            // one weight scale per (row, group), shared by both tokens of the
+            // fragment; s_a is applied once to the finished sum (rows past N
+            // read row N - 1's scale and are never stored)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int64_t n = b * kBoxRows + (i >> 2) * 8 + 2 * t4 + (i & 1);
-              const int m = g8 + 8 * ((i >> 1) & 1);
-              if (n < N && m < MB) {
-                const float sc = __fmul_rn(s_sa[m], __ldg(p.sw + n * p.G + gi));
-                facc[i] = fmaf(sc, i < 4 ? c0[i] : c1[i - 4], facc[i]);
+            for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                int64_t n = b * kBoxRows + nb * 8 + 2 * t4 + e;
+                n = n < N ? n : N - 1;
+                const float sw = __ldg(p.sw + n * p.G + gi);
+                const float* c = nb ? c1 : c0;
+                facc[4 * nb + e] = fmaf(sw, c[e], facc[4 * nb + e]);
+                facc[4 * nb + 2 + e] = fmaf(sw, c[2 + e], facc[4 * nb + 2 + e]);
               }
             }
           }
@@ -354,6 +360,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
           // one half (one group when gs = 64).  Staged activations are in the packed
           // order [even codes | odd codes] of every 8, matching the nibbles.
           const int cb = kt * (2 * kBoxBytes) + q * 128;
+          // both halves lie in one group unless gs is 64: one drain for the quarter
+          const bool drain_half = PG && (p.gs % 128) != 0;
+          float c0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int k0 = cb + 64 * h + 16 * t4;
@@ -368,26 +377,30 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             }
             const uint32_t av[4] = {al.x, al.y, al.z, al.w}, hv[4] = {ah.x, ah.y, ah.z, ah.w};
             const uint32_t wv0[2] = {w0.x, w0.y}, wv1[2] = {w1.x, w1.y};
-            float c0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int j = 0; j < 2; ++j) {          // packed word j: codes 8 j .. 8 j + 7
-              const uint32_t u0 = wv0[j] ^ 0x88888888u, u1 = wv1[j] ^ 0x88888888u;
-              const uint32_t e0 = offset_nibbles_to_s8x4(u0 & 0x0F0F0F0Fu);
-              const uint32_t o0 = offset_nibbles_to_s8x4((u0 >> 4) & 0x0F0F0F0Fu);
-              const uint32_t e1 = offset_nibbles_to_s8x4(u1 & 0x0F0F0F0Fu);
-              const uint32_t o1 = offset_nibbles_to_s8x4((u1 >> 4) & 0x0F0F0F0Fu);
+              uint32_t we0[2], wo0[2], we1[2], wo1[2];   // rows g8 and 8 + g8: even / odd pairs
+              s4x8_to_h2_eo(wv0[j], we0, wo0);
+              s4x8_to_h2_eo(wv1[j], we1, wo1);
 #pragma unroll
               for (int oe = 0; oe < 2; ++oe) {     // even codes, then odd codes
-                uint32_t a0, a2, a1 = 0u, a3 = 0u, x0, x1, y0, y1;
+                uint32_t a0, a2, a1 = 0u, a3 = 0u;
                 s8x4_to_h2x2(av[2 * j + oe], a0, a2);
                 if (MB == 16) s8x4_to_h2x2(hv[2 * j + oe], a1, a3);
-                s8x4_to_h2x2(oe ? o0 : e0, x0, x1);
-                s8x4_to_h2x2(oe ? o1 : e1, y0, y1);
+                const uint32_t x0 = oe ? wo0[0] : we0[0], x1 = oe ? wo0[1] : we0[1];
+                const uint32_t y0 = oe ? wo1[0] : we1[0], y1 = oe ? wo1[1] : we1[1];
                 mma_16816(c0, a0, a1, a2, a3, x0, x1);
                 mma_16816(c1, a0, a1, a2, a3, y0, y1);
               }
             }
-            drain(c0, c1, PG ? (cb + 64 * h) / p.gs : 0);
+            if (h == 1 || drain_half) {   // sums of 128 products stay far below 2^24: exact
+              drain(c0, c1, PG ? (cb + 64 * h) / p.gs : 0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                c0[i] = 0.0f;
+                c1[i] = 0.0f;
+              }
+            }
           }
         }
       }
@@ -416,6 +429,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             float v = 0.0f;
 #pragma unroll
             for (int w = 0; w < kGemvWarps; ++w) v += __int_as_float(s_red[w][src]);
+            v = __fmul_rn(v, s_sa[m]);
             if (ks > 1)
               p.part[(static_cast<int64_t>(slice) * M + m) * N + n] = __float_as_uint(v);
             else
