@@ -264,10 +264,13 @@ def test_mixed_fast_and_slow_token_tiles(cider, bits, K):
 
 
 @pytest.mark.parametrize("M,N,K,gs,bits", [(1, 264, 1024, 0, 8), (16, 136, 2048, 128, 4),
+                                           (16, 2560, 10240, 0, 8), (16, 2560, 10240, 128, 4),
                                            (300, 264, 1024, 0, 8), (200, 136, 1024, 64, 8)])
 def test_linear_replays_from_cuda_graph(cider, M, N, K, gs, bits):
     """The entry points enqueue only stream-ordered work (kernels, pool
-    allocations), so a captured call replays to the same bits as an eager one."""
+    allocations), so a captured call replays to the same bits as an eager one.
+    The small-M shapes include the quantization -> GEMV -> K-slice combine
+    chain, whose later launches may start before the earlier ones end."""
     x = to_dev(inputs.activations(M, K, seed=90))
     qw_dev, _, sw = make_weights(N, K, gs, bits, seed=91)
     qw_d, sw_d = to_dev(qw_dev), to_dev(sw)

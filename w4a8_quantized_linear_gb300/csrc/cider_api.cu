@@ -300,9 +300,12 @@ cider_status_t run_linear(const LinearArgs& a, ScratchSource& scratch) {
         sa = ss;
       }
     }
+    // the GEMV overlaps the quantization launch just before it, unless a
+    // kernel-timing event is recorded between the two
+    const bool overlap = quantize_first && !t_timer.on;
     return cuda_status(timed_launch(a.st, [&] {
       return launch_gemv(xg, qa, sa, a.M, a.N, a.K, w, a.int4, a.sw, gs, a.mode, y, a.acc, part,
-                         sms, a.st);
+                         sms, a.st, overlap);
     }));
   }
   // tensor-core path: activation codes as fp16 integers, scales, row sums of

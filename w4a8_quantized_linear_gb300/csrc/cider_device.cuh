@@ -264,6 +264,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the kernel before it on the stream still
+// runs; pdl_wait() returns once that kernel has completed and its writes are
+// visible (at once when the launch had no such attribute).  The kernel before
+// lets its dependents start early with pdl_launch_dependents().
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -519,6 +529,27 @@ __device__ __forceinline__ void s4x8_to_h2_eo(uint32_t w, uint32_t (&ev)[2], uin
     ev[p] = *reinterpret_cast<const uint32_t*>(&rl);
     od[p] = *reinterpret_cast<const uint32_t*>(&rh);
   }
+}
+
+// Eight int8 codes in natural order (lo: codes 0..3, hi: codes 4..7) as
+// fp16 pairs of even codes {c0, c2} {c4, c6} and of odd codes {c1, c3}
+// {c5, c7}, exactly: the byte permutes that place each code in the mantissa
+// of 1024 (offset binary, code + 128; minus 1152) also pick the even / odd codes.
+__device__ __forceinline__ void s8x8_to_h2_eo(uint32_t lo, uint32_t hi, uint32_t (&ev)[2],
+                                              uint32_t (&od)[2]) {
+  const uint32_t l = lo ^ 0x80808080u, h = hi ^ 0x80808080u;
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));
+  uint32_t r[4] = {__byte_perm(l, 0x64646464u, 0x5240u), __byte_perm(h, 0x64646464u, 0x5240u),
+                   __byte_perm(l, 0x64646464u, 0x5341u), __byte_perm(h, 0x64646464u, 0x5341u)};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 v = __hsub2(*reinterpret_cast<__half2*>(&r[i]), bias);
+    r[i] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  ev[0] = r[0];
+  ev[1] = r[1];
+  od[0] = r[2];
+  od[1] = r[3];
 }
 
 // x / s correctly rounded (IEEE binary32, round to nearest even), from

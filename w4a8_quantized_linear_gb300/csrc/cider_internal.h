@@ -85,9 +85,12 @@ size_t gemv_part_bytes(int64_t M, int64_t N, int64_t K, bool int4, int group_siz
 // The number of K slices it uses (1: none).  Host arithmetic only.
 int gemv_slices(int64_t M, int64_t N, int64_t K, bool int4, int group_size, int mode,
                 int num_sms);
+// after_quant: the launch just before on `st` is this library's activation
+// quantization, which the GEMV may overlap (programmatic dependent launch).
 cudaError_t launch_gemv(const __half* x, const int8_t* qa, const float* sa, int64_t M, int64_t N,
                         int64_t K, const uint8_t* w, bool int4, const float* sw, int group_size,
-                        int mode, __half* y, int32_t* acc, void* part, int num_sms, cudaStream_t st);
+                        int mode, __half* y, int32_t* acc, void* part, int num_sms, cudaStream_t st,
+                        bool after_quant);
 
 // gemm_tc.cu: tensor-core path.  qa16 holds the activation codes as fp16
 // integers [M, K]; row_l1[m] = sum_k |code| (used by the per-channel kernel

@@ -40,6 +40,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 #include <cuda.h>
 
 #include "cider_device.cuh"
@@ -87,6 +88,7 @@ struct GemvArgs {
   const float* sw;
   int gs, G, NS;
   int ks, tps, Ka;    // K slices, tiles per slice, staged codes per token row
+  int P;              // row pitch of the staged codes (bytes; >= Ka)
   __half* y;
   int32_t* acc;
   uint32_t* part;     // ks > 1: partial sums [ks][M][N] (int32 per channel, fp32 per group)
@@ -114,6 +116,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   uint8_t* s_act = smem + static_cast<size_t>(p.NS) * kTileBytes;
   __shared__ __align__(8) uint64_t s_full[kRingMax];
   __shared__ __align__(8) uint64_t s_empty[kRingMax];
+  __shared__ __align__(8) uint64_t s_actbar;   // tensor-core form: the rows' bulk copies
   __shared__ float s_sa[16];
   __shared__ float s_rcp[16];
   __shared__ unsigned s_amax[16];
@@ -135,7 +138,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   const int kt0 = slice * p.tps;
   const int kt1 = kt0 + p.tps < ntk ? kt0 + p.tps : ntk;
   const int kbase = kt0 * kCodesPerTile;   // first code of the slice
-  const int Ka = p.Ka;                     // row stride of the staged codes
+  const int Ka = p.Ka;                     // staged codes per token row
+  const int P = p.P;                       // their row pitch in shared memory
+  // the tensor-core form takes prequantized rows by bulk copies, in natural
+  // order (its INT4 converter picks even / odd codes itself)
+  constexpr bool kBulkAct = MMA && !FUSEQ;
+  const int act_bytes = Ka < K - kbase ? Ka : K - kbase;   // copied per row (a multiple of 32)
 
   if (threadIdx.x == 0) {
     s_abort = 0u;
@@ -143,9 +151,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       mbar_init(smem_u32(&s_full[i]), 1);
       mbar_init(smem_u32(&s_empty[i]), MMA ? kGemvWarps / 2 : kGemvWarps);
     }
+    mbar_init(smem_u32(&s_actbar), 1);
     fence_mbar_init();
   }
   __syncthreads();
+  if (ks > 1) pdl_launch_dependents();   // the combine launch may start now
 
   if (warp == kGemvWarps) {
     // ------------------------------------------------------------ producer
@@ -154,6 +164,18 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     // GB300, however many are in flight), so each slot gets its own issuer.
     if (lane == 0) prefetch_tensormap(&tmW);
     __syncwarp();
+    if (kBulkAct && lane == 31) {
+      // one bulk copy per token row of the slice's codes (q_a and its rows
+      // start on 16-byte boundaries, K % 32 == 0); the rest stays zero.  The
+      // codes may come from the launch before this one: wait for it (the
+      // weight tiles above do not depend on it)
+      pdl_wait();
+      const uint32_t bar = smem_u32(&s_actbar);
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(M * act_bytes));
+      for (int m = 0; m < M; ++m)
+        bulk_load(smem_u32(s_act + static_cast<size_t>(m) * P), p.qa + static_cast<int64_t>(m) * K + kbase,
+                  static_cast<uint32_t>(act_bytes), bar);
+    }
     if (lane < NS) {
       int it = 0;
       for (int64_t b = b_first; b < nblocks; b += b_step)
@@ -174,6 +196,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   // ------------------------------------------------------------ consumers
   const int cthreads = kGemvWarps * 32;
   const int ctid = threadIdx.x;
+  pdl_wait();   // rows, codes and scales may come from the launch before this one
   if (FUSEQ) {
     // per-token amax (|x| >= 0, so its float bits order like unsigned
     // integers), then the codes; x is [M, K] row-major, vector i is row i/nvec
@@ -256,11 +279,20 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
               word[q] = (static_cast<uint32_t>(c0 & 0xFF)) | (static_cast<uint32_t>(c1 & 0xFF) << 8) |
                         (static_cast<uint32_t>(c2 & 0xFF) << 16) | (static_cast<uint32_t>(c3 & 0xFF) << 24);
             }
-            out = arrange8<INT4>(word[0], word[1]);
+            out = arrange8<INT4 && !MMA>(word[0], word[1]);
           }
-          reinterpret_cast<uint2*>(s_act)[i] = out;
+          const int m = i / nvec;
+          *reinterpret_cast<uint2*>(s_act + static_cast<size_t>(m) * P + 8 * (i - m * nvec)) = out;
         }
       }
+    }
+  } else if (kBulkAct) {
+    // zeros where no copy lands: rows past M, and codes past K in a row
+    const int tail16 = (Ka - act_bytes) / 16;
+    for (int i = ctid; i < MB * (Ka / 16); i += cthreads) {
+      const int m = i / (Ka / 16), c = i - m * (Ka / 16);
+      if (m >= M || c >= (Ka / 16) - tail16)
+        *reinterpret_cast<uint4*>(s_act + static_cast<size_t>(m) * P + c * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
   } else {
     // codes [kbase, kbase + Ka) of every token row (zeros past K and past M)
@@ -271,8 +303,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       if (m < M && kbase + c * 16 < K)
         v = *reinterpret_cast<const uint4*>(p.qa + static_cast<int64_t>(m) * K + kbase + c * 16);
       const uint2 a = arrange8<INT4>(v.x, v.y), b = arrange8<INT4>(v.z, v.w);
-      *reinterpret_cast<uint4*>(s_act + static_cast<size_t>(m) * Ka + c * 16) = make_uint4(a.x, a.y, b.x, b.y);
+      *reinterpret_cast<uint4*>(s_act + static_cast<size_t>(m) * P + c * 16) = make_uint4(a.x, a.y, b.x, b.y);
     }
+  }
+  if (!FUSEQ) {
     if (ctid < MB) s_sa[ctid] = (p.sa != nullptr && ctid < M) ? p.sa[ctid] : 0.0f;
   }
   named_barrier_sync(1, cthreads);
@@ -286,8 +320,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     // fragment k order: in k-step j, thread t4 holds codes 16 t4 + 4 j .. + 3
     // of its quarter for both operands (the same permutation of K for A and B)
     // staged rows start at code kbase: the code at k lives at row + (k - kbase)
-    const uint8_t* arow0 = s_act + static_cast<size_t>(g8) * Ka;
-    const uint8_t* arow1 = s_act + static_cast<size_t>(g8 + 8) * Ka;
+    const uint8_t* arow0 = s_act + static_cast<size_t>(g8) * P;
+    const uint8_t* arow1 = s_act + static_cast<size_t>(g8 + 8) * P;
+    if (kBulkAct && !__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&s_actbar), 0u, &s_abort, p.err,
+                                                               kKernelWaitTimeoutNs)))
+      return;
     int it = 0;
     for (int64_t b = b_first; b < nblocks; b += b_step) {
       int iacc[8];    // [n-block][4]: tokens g8 (0, 1) / g8 + 8 (2, 3), rows 2 t4 (+1)
@@ -357,8 +394,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         } else {
           // the quarter holds 128 codes in two 64-code halves; thread t4 holds codes
           // 16 t4 .. + 15 of each half (8 packed bytes), so every k-step stays inside
-          // one half (one group when gs = 64).  Staged activations are in the packed
-          // order [even codes | odd codes] of every 8, matching the nibbles.
+          // one half (one group when gs = 64).  A packed word's low nibbles are its
+          // even codes: each 8 codes go through two k-steps, even codes then odd.
           const int cb = kt * (2 * kBoxBytes) + q * 128;
           // both halves lie in one group unless gs is 64: one drain for the quarter
           const bool drain_half = PG && (p.gs % 128) != 0;
@@ -382,16 +419,13 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
               uint32_t we0[2], wo0[2], we1[2], wo1[2];   // rows g8 and 8 + g8: even / odd pairs
               s4x8_to_h2_eo(wv0[j], we0, wo0);
               s4x8_to_h2_eo(wv1[j], we1, wo1);
-#pragma unroll
-              for (int oe = 0; oe < 2; ++oe) {     // even codes, then odd codes
-                uint32_t a0, a2, a1 = 0u, a3 = 0u;
-                s8x4_to_h2x2(av[2 * j + oe], a0, a2);
-                if (MB == 16) s8x4_to_h2x2(hv[2 * j + oe], a1, a3);
-                const uint32_t x0 = oe ? wo0[0] : we0[0], x1 = oe ? wo0[1] : we0[1];
-                const uint32_t y0 = oe ? wo1[0] : we1[0], y1 = oe ? wo1[1] : we1[1];
-                mma_16816(c0, a0, a1, a2, a3, x0, x1);
-                mma_16816(c1, a0, a1, a2, a3, y0, y1);
-              }
+              uint32_t ae[2], ao[2], he[2] = {0u, 0u}, ho[2] = {0u, 0u};   // tokens g8 / 8 + g8
+              s8x8_to_h2_eo(av[2 * j], av[2 * j + 1], ae, ao);
+              if (MB == 16) s8x8_to_h2_eo(hv[2 * j], hv[2 * j + 1], he, ho);
+              mma_16816(c0, ae[0], he[0], ae[1], he[1], we0[0], we0[1]);   // even codes
+              mma_16816(c1, ae[0], he[0], ae[1], he[1], we1[0], we1[1]);
+              mma_16816(c0, ao[0], ho[0], ao[1], ho[1], wo0[0], wo0[1]);   // odd codes
+              mma_16816(c1, ao[0], ho[0], ao[1], ho[1], wo1[0], wo1[1]);
             }
             if (h == 1 || drain_half) {   // sums of 128 products stay far below 2^24: exact
               drain(c0, c1, PG ? (cb + 64 * h) / p.gs : 0);
@@ -485,7 +519,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         uint4 a0 = make_uint4(0u, 0u, 0u, 0u), a1 = a0;
         if (live) {
           // staged rows start at code kbase
-          const uint8_t* ap = s_act + static_cast<size_t>(m) * Ka + (c * VALS - kbase);
+          const uint8_t* ap = s_act + static_cast<size_t>(m) * P + (c * VALS - kbase);
           a0 = *reinterpret_cast<const uint4*>(ap);
           if (INT4) a1 = *reinterpret_cast<const uint4*>(ap + 16);
         }
@@ -549,8 +583,13 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 }  // dp4a form
 }
 
+// Row pitch of the staged codes: in the tensor-core form a quarter-warp's
+// 16-byte loads cover 64 bytes of each of two token rows, so the rows start
+// 64 bytes apart modulo 128 and the two halves fall in different banks.
+int64_t act_pitch(int64_t Ka, bool mma) { return mma ? (Ka + 127) / 128 * 128 + 64 : Ka; }
+
 int ring_slots(int64_t MB, int64_t K, bool mma = false) {
-  const int64_t room = kSmemBudget - (mma ? kRedBytes : 0) - MB * K;
+  const int64_t room = kSmemBudget - (mma ? kRedBytes : 0) - MB * act_pitch(K, mma);
   int64_t ns = room / kTileBytes;
   if (ns > kRingMax) ns = kRingMax;
   return static_cast<int>(ns);
@@ -566,6 +605,7 @@ __global__ void __launch_bounds__(256) gemv_combine_kernel(const uint32_t* __res
                                                            const float* __restrict__ sw,
                                                            __half* __restrict__ y) {
   const int64_t total = static_cast<int64_t>(M) * N;
+  pdl_wait();   // the partials are the GEMV's, launched just before
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int m = static_cast<int>(i / N);
@@ -604,7 +644,7 @@ GemvSplit gemv_plan(int64_t MB, int64_t N, int64_t K, bool int4, bool mma, bool 
   auto cost = [&](int tps, int kse, int Ka) {
     int ns = ring_slots(MB, Ka, mma);
     if (ns > 8) ns = 8;
-    const int64_t sm = static_cast<int64_t>(ns) * kTileBytes + MB * Ka + 1024;
+    const int64_t sm = static_cast<int64_t>(ns) * kTileBytes + MB * act_pitch(Ka, mma) + 1024;
     int64_t occ = (228 * 1024) / (sm + (mma ? kRedBytes : 0) + 2 * 1024);
     const int64_t cap = mma ? 2 : 4;
     if (occ > cap) occ = cap;
@@ -633,18 +673,37 @@ GemvSplit gemv_plan(int64_t MB, int64_t N, int64_t K, bool int4, bool mma, bool 
   return best;
 }
 
+// A launch that, when `dependent`, may begin before the launch before it on
+// the stream has finished (the kernel waits for it with pdl_wait()).
+template <typename... Params, typename... Args>
+cudaError_t launch_maybe_dependent(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                                   cudaStream_t st, bool dependent, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 template <int MB, bool INT4, bool PG, int EPI, bool FUSEQ, bool MMA>
 cudaError_t launch_one(const __half* x, const int8_t* qa, const float* sa, int64_t M, int64_t N,
                        int64_t K, const uint8_t* w, const float* sw, int gs, __half* y,
                        int32_t* acc, const GemvSplit& sp, uint32_t* part, int num_sms,
-                       cudaStream_t st) {
+                       cudaStream_t st, bool after_quant) {
   auto kern = gemv_kernel<MB, INT4, PG, EPI, FUSEQ, MMA>;
   const int room = ring_slots(MB, sp.Ka, MMA);
   if (room < 4) return cudaErrorInvalidValue;
   // enough slots for every tile of a (row block, slice) when that is more
   // than four: then all of a CTA's weight tiles are requested at once
   const int NS = room < (sp.tps > 4 ? sp.tps : 4) ? room : (sp.tps > 4 ? sp.tps : 4);
-  const size_t smem = static_cast<size_t>(NS) * kTileBytes + static_cast<size_t>(MB) * sp.Ka + 1024;
+  const int64_t pitch = act_pitch(sp.Ka, MMA);
+  const size_t smem = static_cast<size_t>(NS) * kTileBytes + static_cast<size_t>(MB * pitch) + 1024;
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern),
                                           kSmemBudget - (MMA ? kRedBytes : 0) + 1024, attr_done);
@@ -668,6 +727,7 @@ cudaError_t launch_one(const __half* x, const int8_t* qa, const float* sa, int64
   a.ks = sp.ks;
   a.tps = sp.tps;
   a.Ka = sp.Ka;
+  a.P = static_cast<int>(pitch);
   a.y = y;
   a.acc = acc;
   a.part = part;
@@ -693,14 +753,17 @@ cudaError_t launch_one(const __half* x, const int8_t* qa, const float* sa, int64
   int64_t blocks = nblocks * sp.ks;   // (row block, slice) units
   const int64_t cap = static_cast<int64_t>(num_sms) * occ;
   if (blocks > cap) blocks = cap / sp.ks * sp.ks;   // every CTA keeps one slice
-  kern<<<static_cast<unsigned>(blocks), kGemvThreads, smem, st>>>(tmW, a);
-  e = cudaGetLastError();
+  // after this library's own quantization launch the GEMV may start early
+  // (programmatic dependent launch): its weight stream does not depend on the
+  // codes, and it waits for them before reading them
+  e = launch_maybe_dependent(kern, dim3(static_cast<unsigned>(blocks)), dim3(kGemvThreads), smem, st,
+                             after_quant, tmW, a);
   if (e != cudaSuccess || sp.ks == 1) return e;
   const int64_t total = M * N;
   const unsigned cb = static_cast<unsigned>((total + 255) / 256 < 1024 ? (total + 255) / 256 : 1024);
-  gemv_combine_kernel<PG, PG && MMA, EPI == kEpiYb><<<cb, 256, 0, st>>>(part, sp.ks, static_cast<int>(M), N, sa,
-                                                         sw, y);
-  return cudaGetLastError();
+  return launch_maybe_dependent(gemv_combine_kernel<PG, PG && MMA, EPI == kEpiYb>, dim3(cb), dim3(256), 0,
+                                st, true, static_cast<const uint32_t*>(part), sp.ks, static_cast<int>(M),
+                                N, sa, sw, y);
 }
 
 // The tensor-core form serves 4..16 tokens, int8 or int4 weights (not the
@@ -712,7 +775,8 @@ bool gemv_uses_mma(int64_t MB, int64_t K, bool pg, int mode) {
 template <int MB>
 cudaError_t dispatch_mb(const __half* x, const int8_t* qa, const float* sa, int64_t M, int64_t N,
                         int64_t K, const uint8_t* w, bool int4, const float* sw, int gs, int mode,
-                        __half* y, int32_t* acc, uint32_t* part, int num_sms, cudaStream_t st) {
+                        __half* y, int32_t* acc, uint32_t* part, int num_sms, cudaStream_t st,
+                        bool after_quant) {
   const bool pg = gs > 0;
   const bool fq = x != nullptr;
   constexpr bool kMmaMB = MB >= 4;
@@ -723,7 +787,7 @@ cudaError_t dispatch_mb(const __half* x, const int8_t* qa, const float* sa, int6
 #define CIDER_GEMV_MMA_CASE(I4, P, E, F)                                                      \
   if (int4 == I4 && pg == P && mode == E && fq == F)                                          \
     return launch_one<MB, I4, P, E, F, kMmaMB>(x, qa, sa, M, N, K, w, sw, gs, y, acc, sp, part,    \
-                                               num_sms, st);
+                                               num_sms, st, after_quant);
     CIDER_GEMV_MMA_CASE(false, false, kEpiY, true)
     CIDER_GEMV_MMA_CASE(false, true, kEpiY, true)
     CIDER_GEMV_MMA_CASE(false, false, kEpiY, false)
@@ -743,7 +807,7 @@ cudaError_t dispatch_mb(const __half* x, const int8_t* qa, const float* sa, int6
 #define CIDER_GEMV_CASE(I4, P, E, F)                                                          \
   if (int4 == I4 && pg == P && mode == E && fq == F)                                          \
     return launch_one<MB, I4, P, E, F, false>(x, qa, sa, M, N, K, w, sw, gs, y, acc, sp, part,     \
-                                              num_sms, st);
+                                              num_sms, st, after_quant);
   CIDER_GEMV_CASE(false, false, kEpiY, true)
   CIDER_GEMV_CASE(false, true, kEpiY, true)
   CIDER_GEMV_CASE(true, false, kEpiY, true)
@@ -789,13 +853,14 @@ size_t gemv_part_bytes(int64_t M, int64_t N, int64_t K, bool int4, int group_siz
 
 cudaError_t launch_gemv(const __half* x, const int8_t* qa, const float* sa, int64_t M, int64_t N,
                         int64_t K, const uint8_t* w, bool int4, const float* sw, int group_size,
-                        int mode, __half* y, int32_t* acc, void* part, int num_sms, cudaStream_t st) {
+                        int mode, __half* y, int32_t* acc, void* part, int num_sms, cudaStream_t st,
+                        bool after_quant) {
   uint32_t* pp = static_cast<uint32_t*>(part);
-  if (M <= 1) return dispatch_mb<1>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, pp, num_sms, st);
-  if (M <= 2) return dispatch_mb<2>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, pp, num_sms, st);
-  if (M <= 4) return dispatch_mb<4>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, pp, num_sms, st);
-  if (M <= 8) return dispatch_mb<8>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, pp, num_sms, st);
-  return dispatch_mb<16>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, pp, num_sms, st);
+  if (M <= 1) return dispatch_mb<1>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, pp, num_sms, st, after_quant);
+  if (M <= 2) return dispatch_mb<2>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, pp, num_sms, st, after_quant);
+  if (M <= 4) return dispatch_mb<4>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, pp, num_sms, st, after_quant);
+  if (M <= 8) return dispatch_mb<8>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, pp, num_sms, st, after_quant);
+  return dispatch_mb<16>(x, qa, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, pp, num_sms, st, after_quant);
 }
 
 }  // namespace cider

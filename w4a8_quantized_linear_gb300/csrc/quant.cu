@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const InT* __r
   __shared__ float red[4];
   __shared__ int ired[4];
   const int64_t m = blockIdx.x;
+  pdl_launch_dependents();   // a dependent GEMV may start its weight stream now
   clear_words(zero, zero_words);
   const uint4* row = reinterpret_cast<const uint4*>(x + m * K);
   const int nvec = static_cast<int>(K >> 3);
@@ -193,6 +194,7 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_long_kernel(const InT
   __shared__ float red[4];
   __shared__ int ired[4];
   const int64_t m = blockIdx.x;
+  pdl_launch_dependents();
   clear_words(zero, zero_words);
   const uint4* row = reinterpret_cast<const uint4*>(x + m * K);
   const int64_t nvec = K >> 3;
