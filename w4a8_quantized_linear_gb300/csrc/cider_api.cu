@@ -336,9 +336,12 @@ cider_status_t run_linear(const LinearArgs& a, ScratchSource& scratch) {
     e = launch_codes_s8_to_f16(a.qa, a.M, a.K, q16, row_l1, zero, gsc.zero_words, a.st);
   }
   if (e != cudaSuccess) return cuda_status(e);
+  // the GEMM overlaps its set-up with the quantization launch just before it,
+  // unless a kernel-timing event is recorded between the two
+  const bool overlap = !t_timer.on;
   return cuda_status(timed_launch(a.st, [&] {
     return launch_gemm_tc(q16, sa, row_l1, a.M, a.N, a.K, w, a.int4, a.sw, gs, a.mode, y, a.acc,
-                          ws, sms, a.st);
+                          ws, sms, a.st, overlap);
   }));
 }
 

@@ -108,16 +108,17 @@ GemmScratch gemm_tc_scratch(int64_t M, int64_t N, int64_t K, int group_size);
 cudaError_t launch_gemm_tc(const __half* qa16, const float* sa, const int* row_l1, int64_t M,
                            int64_t N, int64_t K, const uint8_t* w, bool int4, const float* sw,
                            int group_size, int mode, __half* y, int32_t* acc, void* workspace,
-                           int num_sms, cudaStream_t st);
+                           int num_sms, cudaStream_t st, bool after_quant);
 // gemm_pg.cu: per-group tensor-core path on CTA pairs (see launch_gemm_tc).
 cudaError_t launch_gemm_pg(const __half* qa16, const float* sa, int64_t M, int64_t N, int64_t K,
                            const uint8_t* w, bool int4, const float* sw, int group_size, int mode,
-                           __half* y, int32_t* acc, cudaStream_t st);
+                           __half* y, int32_t* acc, cudaStream_t st, bool after_quant);
 // gemm_pair.cu: per-channel tensor-core path on CTA pairs (see launch_gemm_tc).
 GemmScratch gemm_pair_scratch(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_pair(const __half* qa16, const float* sa, const int* row_l1, int64_t M,
                              int64_t N, int64_t K, const uint8_t* w, bool int4, const float* sw,
-                             int mode, __half* y, int32_t* acc, void* workspace, cudaStream_t st);
+                             int mode, __half* y, int32_t* acc, void* workspace, cudaStream_t st,
+                             bool after_quant);
 // Host copy of the pair GEMM's work split (see cider_debug_pair_schedule).
 void pair_schedule(int64_t M, int64_t N, int64_t K, int pairs, int64_t capacity, int32_t* units,
                    int64_t* count, int32_t* info);

@@ -297,6 +297,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   __syncthreads();
   cluster_sync_all();   // barriers of both CTAs initialised, tensor memory held
   tc_fence_after();
+  pdl_wait();   // codes, scales and flags come from the quantization launch just before
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + C::kBarOffset + 8 * C::kNumBars);
   const int nu = pair_num_units(p, cid, nclusters);
 
@@ -820,29 +821,35 @@ size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 // the runtime then starts it only with every CTA pair resident at once (or
 // fails the launch), so no piece can wait on a partner that other work on
 // the GPU keeps from starting.  The bounded waits stay as a backstop.
+// After this library's quantization launch the kernel may also start before
+// that launch ends (programmatic dependent launch): it sets up its barriers
+// and tensor memory, then waits for the codes.
 template <bool INT4, int EPI>
 cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmW, const PairArgs& a,
-                        int clusters, cudaStream_t st) {
+                        int clusters, cudaStream_t st, bool after_quant) {
   using C = PCfg<INT4>;
   auto kern = gemm_pair_kernel<INT4, EPI>;
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::kSmemBytes,
                                           attr_done);
   if (e != cudaSuccess) return e;
-  if (a.sk_tiles == 0) {
-    kern<<<2 * clusters, kPThreads, C::kSmemBytes, st>>>(tmX, tmW, a);
-    return cudaGetLastError();
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
   cfg.blockDim = dim3(kPThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (a.sk_tiles > 0) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n++].val.cooperative = 1;
+  }
+  if (after_quant) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n++].val.programmaticStreamSerializationAllowed = 1;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, tmX, tmW, a);
 }
 
@@ -901,7 +908,8 @@ GemmScratch gemm_pair_scratch(int64_t M, int64_t N, int64_t K) {
 
 cudaError_t launch_gemm_pair(const __half* qa16, const float* sa, const int* row_l1, int64_t M,
                              int64_t N, int64_t K, const uint8_t* w, bool int4, const float* sw,
-                             int mode, __half* y, int32_t* acc, void* workspace, cudaStream_t st) {
+                             int mode, __half* y, int32_t* acc, void* workspace, cudaStream_t st,
+                             bool after_quant) {
   CUtensorMap tmX, tmW;
   if (!make_tensor_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qa16, K, M, K * 2, kPSubK, kPHalf,
                           CU_TENSOR_MAP_SWIZZLE_128B))
@@ -938,12 +946,12 @@ cudaError_t launch_gemm_pair(const __half* qa16, const float* sa, const int* row
   e = device_error_word(&a.err);
   if (e != cudaSuccess) return e;
   if (int4)
-    return mode == kEpiY    ? launch_pair<true, kEpiY>(tmX, tmW, a, pl.clusters, st)
-           : mode == kEpiYb ? launch_pair<true, kEpiYb>(tmX, tmW, a, pl.clusters, st)
-                            : launch_pair<true, kEpiAcc>(tmX, tmW, a, pl.clusters, st);
-  return mode == kEpiY    ? launch_pair<false, kEpiY>(tmX, tmW, a, pl.clusters, st)
-         : mode == kEpiYb ? launch_pair<false, kEpiYb>(tmX, tmW, a, pl.clusters, st)
-                          : launch_pair<false, kEpiAcc>(tmX, tmW, a, pl.clusters, st);
+    return mode == kEpiY    ? launch_pair<true, kEpiY>(tmX, tmW, a, pl.clusters, st, after_quant)
+           : mode == kEpiYb ? launch_pair<true, kEpiYb>(tmX, tmW, a, pl.clusters, st, after_quant)
+                            : launch_pair<true, kEpiAcc>(tmX, tmW, a, pl.clusters, st, after_quant);
+  return mode == kEpiY    ? launch_pair<false, kEpiY>(tmX, tmW, a, pl.clusters, st, after_quant)
+         : mode == kEpiYb ? launch_pair<false, kEpiYb>(tmX, tmW, a, pl.clusters, st, after_quant)
+                          : launch_pair<false, kEpiAcc>(tmX, tmW, a, pl.clusters, st, after_quant);
 }
 
 }  // namespace cider

@@ -248,6 +248,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();   // barriers of both CTAs initialised, tensor memory held
+  pdl_wait();   // codes and scales come from the quantization launch just before
   tc_fence_after();
   const uint32_t tmem =
       *reinterpret_cast<volatile uint32_t*>(gbase + C::kBarOffset + 8 * C::kNumBars);
@@ -633,9 +634,11 @@ cudaError_t pg_max_clusters(int* out) {
   return cudaSuccess;
 }
 
+// after_quant: may start before this library's quantization launch just
+// before it ends (programmatic dependent launch; the kernel waits for it).
 template <bool INT4, int EPI, bool BATCH>
 cudaError_t launch_pg(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap& tmY,
-                      const PgArgs& a, int clusters, cudaStream_t st) {
+                      const PgArgs& a, int clusters, cudaStream_t st, bool after_quant) {
   using C = GCfg<INT4>;
   auto kern = gemm_pg_kernel<INT4, EPI, BATCH>;
   static std::atomic<uint64_t> attr_done{0};
@@ -653,15 +656,24 @@ cudaError_t launch_pg(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUte
     regs_ok.store(fa.numRegs * kGThreads >= kGRegsNeeded ? 1 : -1, std::memory_order_relaxed);
   }
   if (regs_ok.load(std::memory_order_relaxed) < 0) return cudaErrorInvalidConfiguration;
-  kern<<<2 * clusters, kGThreads, C::kSmemBytes, st>>>(tmX, tmW, tmY, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+  cfg.blockDim = dim3(kGThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_quant ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, tmX, tmW, tmY, a);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_pg(const __half* qa16, const float* sa, int64_t M, int64_t N, int64_t K,
                            const uint8_t* w, bool int4, const float* sw, int group_size, int mode,
-                           __half* y, int32_t* acc, cudaStream_t st) {
+                           __half* y, int32_t* acc, cudaStream_t st, bool after_quant) {
   if (group_size != 64 && group_size != 128) return cudaErrorInvalidValue;
   CUtensorMap tmX, tmW;
   if (!make_tensor_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qa16, K, M, K * 2, kGSubK, kGHalf,
@@ -700,9 +712,9 @@ cudaError_t launch_gemm_pg(const __half* qa16, const float* sa, int64_t M, int64
   if (e != cudaSuccess) return e;
   const int clusters = a.num_tiles < nc ? a.num_tiles : nc;
 #define CIDER_PG_LAUNCH(I4, B)                                                               \
-  return mode == kEpiY    ? launch_pg<I4, kEpiY, B>(tmX, tmW, tmY, a, clusters, st)          \
-         : mode == kEpiYb ? launch_pg<I4, kEpiYb, B>(tmX, tmW, tmY, a, clusters, st)         \
-                          : launch_pg<I4, kEpiAcc, B>(tmX, tmW, tmY, a, clusters, st);
+  return mode == kEpiY    ? launch_pg<I4, kEpiY, B>(tmX, tmW, tmY, a, clusters, st, after_quant)          \
+         : mode == kEpiYb ? launch_pg<I4, kEpiYb, B>(tmX, tmW, tmY, a, clusters, st, after_quant)         \
+                          : launch_pg<I4, kEpiAcc, B>(tmX, tmW, tmY, a, clusters, st, after_quant);
   if (int4) {
     if (group_size == 128) CIDER_PG_LAUNCH(true, true)
     CIDER_PG_LAUNCH(true, false)

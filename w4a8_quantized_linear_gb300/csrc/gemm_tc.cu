@@ -70,11 +70,12 @@ bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* pt
 cudaError_t launch_gemm_tc(const __half* qa16, const float* sa, const int* row_l1, int64_t M,
                            int64_t N, int64_t K, const uint8_t* w, bool int4, const float* sw,
                            int group_size, int mode, __half* y, int32_t* acc, void* workspace,
-                           int num_sms, cudaStream_t st) {
+                           int num_sms, cudaStream_t st, bool after_quant) {
   (void)num_sms;
   if (group_size == 0)
-    return launch_gemm_pair(qa16, sa, row_l1, M, N, K, w, int4, sw, mode, y, acc, workspace, st);
-  return launch_gemm_pg(qa16, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, st);
+    return launch_gemm_pair(qa16, sa, row_l1, M, N, K, w, int4, sw, mode, y, acc, workspace, st,
+                            after_quant);
+  return launch_gemm_pg(qa16, sa, M, N, K, w, int4, sw, group_size, mode, y, acc, st, after_quant);
 }
 
 GemmScratch gemm_tc_scratch(int64_t M, int64_t N, int64_t K, int group_size) {

@@ -445,6 +445,7 @@ __global__ void __launch_bounds__(kQuantThreads) codes_s8_to_f16_kernel(const in
                                                                         int zero_words) {
   __shared__ int ired[4];
   const int64_t m = blockIdx.x;
+  pdl_launch_dependents();
   clear_words(zero, zero_words);
   const int64_t n16 = K / 16;
   int l1 = 0;
