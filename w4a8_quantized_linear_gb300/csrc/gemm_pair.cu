@@ -652,7 +652,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           }
         }
       }
-      if (piece) {
+      // A CTA whose 128 token rows all lie past M (the second half of a
+      // tile row at M <= 128) has no partial to share and nothing to store;
+      // the other pieces' CTAs of the same half skip the exchange as well.
+      if (piece && mt * kPTileM + static_cast<int>(rank) * kPHalf < p.M) {
         // every lane counts its own stores of the partial
         gpu_count_release(p.flags + (cid * 2 + rank) * 4 + q);
         const int s = p.sk_split, k = cid % s, c0 = cid - k;
