@@ -33,6 +33,12 @@
  *     enqueued on it; no entry point synchronizes.  Launch errors are returned
  *     as CIDER_ERR_CUDA; faults inside kernels surface at the caller's next
  *     synchronization, as with any CUDA library.
+ *   - A linear may enqueue two or three kernels; the later ones are
+ *     programmatic dependent launches that start before the earlier ones end
+ *     and wait for their results inside the kernel.  The call's first kernel
+ *     starts after the stream's earlier work has finished, and its last one
+ *     does not release later work early, so the call as a whole is ordered on
+ *     the stream like a single kernel.
  *   - Argument checks run on the host before any launch, in this order:
  *     an empty problem (M == 0 or N == 0) returns CIDER_OK and launches
  *     nothing; null pointers, negative sizes, K < 32, K % 32 != 0, N % 8 != 0,

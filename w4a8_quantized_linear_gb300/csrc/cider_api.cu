@@ -282,6 +282,9 @@ cider_status_t run_linear(const LinearArgs& a, ScratchSource& scratch) {
         a.x && (a.x_bf16 || a.mode == kEpiYb || pbytes > 0 || !gemv_quantizes_itself(a.M, a.K));
     const size_t qbytes = quantize_first ? round_up(static_cast<size_t>(a.M * a.K), 256) : 0;
     const size_t sbytes = quantize_first ? round_up(4 * a.M, 256) : 0;
+    // the GEMV overlaps the quantization launch just before it, unless a
+    // kernel-timing event is recorded between the two
+    const bool overlap = quantize_first && !t_timer.on;
     if (qbytes + sbytes + pbytes > 0) {
       void* sp = nullptr;
       s = scratch.get(qbytes + sbytes + round_up(pbytes, 256), &sp);
@@ -292,17 +295,14 @@ cider_status_t run_linear(const LinearArgs& a, ScratchSource& scratch) {
         int8_t* qs = reinterpret_cast<int8_t*>(base);
         float* ss = reinterpret_cast<float*>(base + qbytes);
         cudaError_t e = a.x_bf16 ? launch_quant_act_s8_bf16(static_cast<const __nv_bfloat16*>(a.x),
-                                                            a.M, a.K, qs, ss, a.st)
-                                 : launch_quant_act_s8(xg, a.M, a.K, qs, ss, a.st);
+                                                            a.M, a.K, qs, ss, a.st, overlap)
+                                 : launch_quant_act_s8(xg, a.M, a.K, qs, ss, a.st, overlap);
         if (e != cudaSuccess) return cuda_status(e);
         xg = nullptr;
         qa = qs;
         sa = ss;
       }
     }
-    // the GEMV overlaps the quantization launch just before it, unless a
-    // kernel-timing event is recorded between the two
-    const bool overlap = quantize_first && !t_timer.on;
     return cuda_status(timed_launch(a.st, [&] {
       return launch_gemv(xg, qa, sa, a.M, a.N, a.K, w, a.int4, a.sw, gs, a.mode, y, a.acc, part,
                          sms, a.st, overlap);
@@ -324,21 +324,22 @@ cider_status_t run_linear(const LinearArgs& a, ScratchSource& scratch) {
   uint8_t* ws = gsc.bytes ? sbase + qbytes + 2 * vbytes : nullptr;
   int* zero = ws ? reinterpret_cast<int*>(ws + gsc.zero_offset) : nullptr;
   const float* sa = a.sa;
+  // the GEMM overlaps its set-up with the quantization launch just before it,
+  // unless a kernel-timing event is recorded between the two
+  const bool overlap = !t_timer.on;
   cudaError_t e;
   if (a.x) {
     float* sscr = reinterpret_cast<float*>(sbase + qbytes);
     e = a.x_bf16 ? launch_quant_act_f16_from_bf16(static_cast<const __nv_bfloat16*>(a.x), a.M, a.K,
-                                                  q16, sscr, row_l1, zero, gsc.zero_words, a.st)
+                                                  q16, sscr, row_l1, zero, gsc.zero_words, a.st,
+                                                  overlap)
                  : launch_quant_act_f16(static_cast<const __half*>(a.x), a.M, a.K, q16, sscr,
-                                        row_l1, zero, gsc.zero_words, a.st);
+                                        row_l1, zero, gsc.zero_words, a.st, overlap);
     sa = sscr;
   } else {
     e = launch_codes_s8_to_f16(a.qa, a.M, a.K, q16, row_l1, zero, gsc.zero_words, a.st);
   }
   if (e != cudaSuccess) return cuda_status(e);
-  // the GEMM overlaps its set-up with the quantization launch just before it,
-  // unless a kernel-timing event is recorded between the two
-  const bool overlap = !t_timer.on;
   return cuda_status(timed_launch(a.st, [&] {
     return launch_gemm_tc(q16, sa, row_l1, a.M, a.N, a.K, w, a.int4, a.sw, gs, a.mode, y, a.acc,
                           ws, sms, a.st, overlap);

@@ -43,19 +43,22 @@ enum EpiMode : int {
   kEpiYb = 2,   // dequantize and store bf16 y [M, N]
 };
 
-// quant.cu
+// quant.cu.  release: the library's own GEMM or GEMV is launched next on the
+// stream as a programmatic dependent, and may start as soon as every CTA of
+// the quantization is running (false: later work waits for its completion).
 cudaError_t launch_quant_act_s8(const __half* x, int64_t M, int64_t K, int8_t* q, float* sa,
-                                cudaStream_t st);
+                                cudaStream_t st, bool release = false);
 // fp16 codes for the tensor-core path, plus row_l1[m] = sum_k |q[m,k]|; also
 // clears `zero_words` int32 words at `zero` (the GEMM's flags) on the way.
 cudaError_t launch_quant_act_f16(const __half* x, int64_t M, int64_t K, __half* q, float* sa,
-                                 int* row_l1, int* zero, int zero_words, cudaStream_t st);
+                                 int* row_l1, int* zero, int zero_words, cudaStream_t st,
+                                 bool release = false);
 // The same two from bf16 activations.
 cudaError_t launch_quant_act_s8_bf16(const __nv_bfloat16* x, int64_t M, int64_t K, int8_t* q,
-                                     float* sa, cudaStream_t st);
+                                     float* sa, cudaStream_t st, bool release = false);
 cudaError_t launch_quant_act_f16_from_bf16(const __nv_bfloat16* x, int64_t M, int64_t K, __half* q,
                                            float* sa, int* row_l1, int* zero, int zero_words,
-                                           cudaStream_t st);
+                                           cudaStream_t st, bool release = false);
 cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int group_size, bool int4,
                                 uint8_t* q, float* sw, cudaStream_t st);
 // The same with percentile-clipped scales (clip_percentile in (0, 100]).

@@ -147,11 +147,12 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const InT* __r
                                                                   float* __restrict__ sa,
                                                                   int* __restrict__ row_l1,
                                                                   int* __restrict__ zero,
-                                                                  int zero_words) {
+                                                                  int zero_words, bool release) {
   __shared__ float red[4];
   __shared__ int ired[4];
   const int64_t m = blockIdx.x;
-  pdl_launch_dependents();   // a dependent GEMV may start its weight stream now
+  // the library's GEMM / GEMV launched next may start its set-up now
+  if (release) pdl_launch_dependents();
   clear_words(zero, zero_words);
   const uint4* row = reinterpret_cast<const uint4*>(x + m * K);
   const int nvec = static_cast<int>(K >> 3);
@@ -190,11 +191,11 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_long_kernel(const InT
                                                                        float* __restrict__ sa,
                                                                        int* __restrict__ row_l1,
                                                                        int* __restrict__ zero,
-                                                                       int zero_words) {
+                                                                       int zero_words, bool release) {
   __shared__ float red[4];
   __shared__ int ired[4];
   const int64_t m = blockIdx.x;
-  pdl_launch_dependents();
+  if (release) pdl_launch_dependents();
   clear_words(zero, zero_words);
   const uint4* row = reinterpret_cast<const uint4*>(x + m * K);
   const int64_t nvec = K >> 3;
@@ -215,28 +216,28 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_long_kernel(const InT
 
 template <typename OutT, typename InT>
 cudaError_t launch_quant_act(const InT* x, int64_t M, int64_t K, OutT* q, float* sa,
-                             int* row_l1, int* zero, int zero_words, cudaStream_t st) {
+                             int* row_l1, int* zero, int zero_words, cudaStream_t st, bool release) {
   const int64_t nvec = K / 8;
   const int vpt = static_cast<int>((nvec + kQuantThreads - 1) / kQuantThreads);
   const dim3 grid(static_cast<unsigned>(M));
   if (vpt <= 1)
-    quant_act_kernel<OutT, 1, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_kernel<OutT, 1, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words, release);
   else if (vpt <= 2)
-    quant_act_kernel<OutT, 2, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_kernel<OutT, 2, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words, release);
   else if (vpt <= 3)
-    quant_act_kernel<OutT, 3, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_kernel<OutT, 3, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words, release);
   else if (vpt <= 4)
-    quant_act_kernel<OutT, 4, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_kernel<OutT, 4, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words, release);
   else if (vpt <= 6)
-    quant_act_kernel<OutT, 6, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_kernel<OutT, 6, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words, release);
   else if (vpt <= 8)
-    quant_act_kernel<OutT, 8, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_kernel<OutT, 8, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words, release);
   else if (vpt <= 12)
-    quant_act_kernel<OutT, 12, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_kernel<OutT, 12, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words, release);
   else if (vpt <= 16)
-    quant_act_kernel<OutT, 16, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_kernel<OutT, 16, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words, release);
   else
-    quant_act_long_kernel<OutT, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words);
+    quant_act_long_kernel<OutT, InT><<<grid, kQuantThreads, 0, st>>>(x, K, q, sa, row_l1, zero, zero_words, release);
   return cudaGetLastError();
 }
 
@@ -506,24 +507,26 @@ cudaError_t launch_int4_from_offset(const uint8_t* src, uint8_t* dst, int64_t nb
 }
 
 cudaError_t launch_quant_act_s8(const __half* x, int64_t M, int64_t K, int8_t* q, float* sa,
-                                cudaStream_t st) {
-  return launch_quant_act<int8_t, __half>(x, M, K, q, sa, nullptr, nullptr, 0, st);
+                                cudaStream_t st, bool release) {
+  return launch_quant_act<int8_t, __half>(x, M, K, q, sa, nullptr, nullptr, 0, st, release);
 }
 
 cudaError_t launch_quant_act_s8_bf16(const __nv_bfloat16* x, int64_t M, int64_t K, int8_t* q,
-                                     float* sa, cudaStream_t st) {
-  return launch_quant_act<int8_t, __nv_bfloat16>(x, M, K, q, sa, nullptr, nullptr, 0, st);
+                                     float* sa, cudaStream_t st, bool release) {
+  return launch_quant_act<int8_t, __nv_bfloat16>(x, M, K, q, sa, nullptr, nullptr, 0, st, release);
 }
 
 cudaError_t launch_quant_act_f16(const __half* x, int64_t M, int64_t K, __half* q, float* sa,
-                                 int* row_l1, int* zero, int zero_words, cudaStream_t st) {
-  return launch_quant_act<__half, __half>(x, M, K, q, sa, row_l1, zero, zero_words, st);
+                                 int* row_l1, int* zero, int zero_words, cudaStream_t st,
+                                 bool release) {
+  return launch_quant_act<__half, __half>(x, M, K, q, sa, row_l1, zero, zero_words, st, release);
 }
 
 cudaError_t launch_quant_act_f16_from_bf16(const __nv_bfloat16* x, int64_t M, int64_t K, __half* q,
                                            float* sa, int* row_l1, int* zero, int zero_words,
-                                           cudaStream_t st) {
-  return launch_quant_act<__half, __nv_bfloat16>(x, M, K, q, sa, row_l1, zero, zero_words, st);
+                                           cudaStream_t st, bool release) {
+  return launch_quant_act<__half, __nv_bfloat16>(x, M, K, q, sa, row_l1, zero, zero_words, st,
+                                                 release);
 }
 
 cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int group_size, bool int4,
