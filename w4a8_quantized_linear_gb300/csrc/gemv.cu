@@ -20,13 +20,19 @@
 //
 // For 4 to 16 tokens the dot products run on the tensor cores (mma.sync
 // m16n8k16, fp16 operands holding the exact codes, fp32 accumulation drained
-// to int32 after every 64 codes, so every partial sum stays below 2^20 and
-// exact; INT4 codes are unpacked to int8 first): each tile is split into four
-// 64-byte quarters, one per warp, and the two sets of four warps take
+// after every 64 codes of int8 weights or 128 of int4 weights (per group at
+// gs 64: every 64), so every partial sum stays far below 2^24 and exact; a
+// packed INT4 word goes straight to fp16 pairs of its even and its odd codes,
+// and the int8 activations are split the same way): each tile is split into
+// four 64-byte quarters, one per warp, and the two sets of four warps take
 // alternate tiles; the warps' partial sums meet in shared memory at the end
-// of each 16-row block.  With dp4a at these M each weight byte costs M / 4
-// instructions plus shared-memory reloads of the activations, which made the
-// kernel compute-bound well below the weight bandwidth.
+// of each 16-row block.  This form takes prequantized rows by one bulk copy
+// per token row, and when the quantization launch precedes it on the stream
+// it is launched as that kernel's programmatic dependent: it streams weights
+// at once and waits (griddepcontrol.wait) before reading codes or scales.
+// With dp4a at these M each weight byte costs M / 4 instructions plus
+// shared-memory reloads of the activations, which made the kernel
+// compute-bound well below the weight bandwidth.
 //
 // For 1 or 2 tokens (dp4a form) consumer warp w owns rows 2w, 2w+1 of a
 // block; lane l works on row 2w + l/16 and its 16-byte chunk l%16 of each
