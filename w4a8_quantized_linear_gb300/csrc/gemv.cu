@@ -112,8 +112,12 @@ struct GemvArgs {
 // on row 2w + l/16 and on its 16-byte chunk l%16 of each tile, accumulating
 // over the tiles of the block, and the 16 lanes of a row are reduced at the
 // block's end.
+// The tensor-core form with int4 weights and per-group scales is built for
+// three CTAs per SM (72 registers instead of ~92): its shared memory allows a
+// third CTA at the sizes it serves, and the extra warps hide its latency
+// chains.  (The int8 per-group form usually has no room for a third CTA.)
 template <int MB, bool INT4, bool PG, int EPI, bool FUSEQ, bool MMA>
-__global__ void __launch_bounds__(kGemvThreads, 1)
+__global__ void __launch_bounds__(kGemvThreads, (MMA && PG && INT4) ? 3 : 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tmW, const GemvArgs p) {
   static_assert(!MMA || (MB >= 4 && !(PG && EPI == kEpiAcc)), "tensor-core form");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
