@@ -319,6 +319,23 @@ cider_status_t cider_debug_wait_timeout(int64_t max_polls, void* stream);
 cider_status_t cider_debug_small_m_slices(int64_t M, int64_t N, int64_t K, int int4,
                                           int group_size, int num_sms, int32_t* slices);
 
+/* Launch sizes of the small-M path, for tests of its shared-memory bounds:
+ * pure host arithmetic, no GPU needed.  For a linear with y output that takes
+ * the weight-streaming kernel (M <= 16 and the rows fit in shared memory),
+ * writes info[0..9] = {token rows padded to a power of two, 1 if the
+ * tensor-core form (4..16 tokens) is used, K slices, weight tiles per slice,
+ * staged activation codes per token row, the staged rows' pitch in bytes,
+ * weight-ring slots, dynamic shared memory bytes, the kernel's cap on them,
+ * codes per weight-tile row}.  split_allowed nonzero: the rows come
+ * pre-quantized and there is scratch for the slices' partial sums (the only
+ * case in which K is split).  In the tensor-core form each token row's codes
+ * of a slice are copied in by one bulk copy of min(staged codes, K - the
+ * slice's first code) bytes.  Returns CIDER_ERR_INVALID_ARGUMENT when the
+ * problem does not take this path, for N, K or num_sms < 1, or a NULL info. */
+cider_status_t cider_debug_small_m_launch(int64_t M, int64_t N, int64_t K, int int4,
+                                          int group_size, int split_allowed, int num_sms,
+                                          int32_t* info);
+
 /* Work split of the per-channel tensor-core GEMM, for inspection and tests:
  * pure host arithmetic, no GPU needed.  For an M x N x K problem on `pairs`
  * CTA pairs (`pairs` >= 1 stands for the device's count), the GEMM's 256 x 256

@@ -72,6 +72,7 @@ def _declare(lib):
         "cider_debug_wait_timeout": ([i64, p], i32),
         "cider_debug_pair_schedule": ([i64, i64, i64, i32, i64, p, p, p], i32),
         "cider_debug_small_m_slices": ([i64, i64, i64, i32, i32, i32, p], i32),
+        "cider_debug_small_m_launch": ([i64, i64, i64, i32, i32, i32, i32, p], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -365,6 +366,18 @@ def cider_debug_pair_schedule(M: int, N: int, K: int, pairs: int):
     keys = ("pairs", "whole_tiles", "cut_tiles", "pieces", "blocks_per_tile", "tiles")
     units = [tuple(rows[7 * i:7 * i + 7]) for i in range(count.value)]
     return dict(zip(keys, list(info))), units
+
+
+def cider_debug_small_m_launch(M: int, N: int, K: int, bits: int, group_size: int,
+                               split_allowed: bool, num_sms: int) -> dict:
+    """Launch sizes of the small-M path for this linear (host arithmetic only)."""
+    info = (ctypes.c_int32 * 10)()
+    _check("cider_debug_small_m_launch",
+           _load().cider_debug_small_m_launch(M, N, K, 1 if bits == 4 else 0, group_size,
+                                              1 if split_allowed else 0, num_sms, info))
+    keys = ("mb", "mma", "slices", "tiles_per_slice", "staged_codes", "pitch", "ring_slots",
+            "smem", "smem_cap", "codes_per_tile")
+    return dict(zip(keys, list(info)))
 
 
 def cider_debug_small_m_slices(M: int, N: int, K: int, bits: int, group_size: int,

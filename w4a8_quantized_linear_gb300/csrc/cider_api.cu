@@ -648,6 +648,17 @@ cider_status_t cider_debug_small_m_slices(int64_t M, int64_t N, int64_t K, int i
   });
 }
 
+cider_status_t cider_debug_small_m_launch(int64_t M, int64_t N, int64_t K, int int4,
+                                          int group_size, int split_allowed, int num_sms,
+                                          int32_t* info) {
+  return guarded([&] {
+    if (M < 1 || N < 1 || K < 1 || num_sms < 1 || info == nullptr || !cider::gemv_fits(M, K))
+      return CIDER_ERR_INVALID_ARGUMENT;
+    cider::gemv_launch_info(M, N, K, int4 != 0, group_size, split_allowed != 0, num_sms, info);
+    return CIDER_OK;
+  });
+}
+
 cider_status_t cider_debug_pair_schedule(int64_t M, int64_t N, int64_t K, int pairs,
                                          int64_t capacity, int32_t* units, int64_t* count,
                                          int32_t* info) {

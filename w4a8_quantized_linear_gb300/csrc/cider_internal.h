@@ -88,6 +88,13 @@ size_t gemv_part_bytes(int64_t M, int64_t N, int64_t K, bool int4, int group_siz
 // The number of K slices it uses (1: none).  Host arithmetic only.
 int gemv_slices(int64_t M, int64_t N, int64_t K, bool int4, int group_size, int mode,
                 int num_sms);
+// Sizes of the GEMV launch for y output (host arithmetic only): info[0..9] =
+// {padded token count, tensor-core form, K slices, weight tiles per slice,
+// staged codes per token row, their row pitch in bytes, ring slots, dynamic
+// shared memory bytes, the launch's cap on it, codes per weight tile row}.
+// split_allowed: the rows come pre-quantized and scratch for partials exists.
+void gemv_launch_info(int64_t M, int64_t N, int64_t K, bool int4, int group_size, bool split_allowed,
+                      int num_sms, int32_t* info);
 // after_quant: the launch just before on `st` is this library's activation
 // quantization, which the GEMV may overlap (programmatic dependent launch).
 cudaError_t launch_gemv(const __half* x, const int8_t* qa, const float* sa, int64_t M, int64_t N,

@@ -683,6 +683,27 @@ GemvSplit gemv_plan(int64_t MB, int64_t N, int64_t K, bool int4, bool mma, bool 
   return best;
 }
 
+// Sizes of one weight-streaming launch: ring slots (enough for every tile of
+// a (row block, slice) when that is more than four, so that all of a CTA's
+// weight tiles are requested at once; fewer than four: it does not fit), the
+// staged rows' pitch and the dynamic shared memory.
+struct GemvSizes {
+  int NS;
+  int64_t pitch;
+  size_t smem;
+};
+
+GemvSizes gemv_sizes(int64_t MB, const GemvSplit& sp, bool mma) {
+  const int room = ring_slots(MB, sp.Ka, mma);
+  const int want = sp.tps > 4 ? sp.tps : 4;
+  GemvSizes z;
+  z.NS = room < want ? room : want;
+  z.pitch = act_pitch(sp.Ka, mma);
+  z.smem = static_cast<size_t>(z.NS > 0 ? z.NS : 0) * kTileBytes + static_cast<size_t>(MB * z.pitch) +
+           1024;
+  return z;
+}
+
 // A launch that, when `dependent`, may begin before the launch before it on
 // the stream has finished (the kernel waits for it with pdl_wait()).
 template <typename... Params, typename... Args>
@@ -707,13 +728,11 @@ cudaError_t launch_one(const __half* x, const int8_t* qa, const float* sa, int64
                        int32_t* acc, const GemvSplit& sp, uint32_t* part, int num_sms,
                        cudaStream_t st, bool after_quant) {
   auto kern = gemv_kernel<MB, INT4, PG, EPI, FUSEQ, MMA>;
-  const int room = ring_slots(MB, sp.Ka, MMA);
-  if (room < 4) return cudaErrorInvalidValue;
-  // enough slots for every tile of a (row block, slice) when that is more
-  // than four: then all of a CTA's weight tiles are requested at once
-  const int NS = room < (sp.tps > 4 ? sp.tps : 4) ? room : (sp.tps > 4 ? sp.tps : 4);
-  const int64_t pitch = act_pitch(sp.Ka, MMA);
-  const size_t smem = static_cast<size_t>(NS) * kTileBytes + static_cast<size_t>(MB * pitch) + 1024;
+  const GemvSizes z = gemv_sizes(MB, sp, MMA);
+  if (z.NS < 4) return cudaErrorInvalidValue;
+  const int NS = z.NS;
+  const int64_t pitch = z.pitch;
+  const size_t smem = z.smem;
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern),
                                           kSmemBudget - (MMA ? kRedBytes : 0) + 1024, attr_done);
@@ -853,6 +872,25 @@ int gemv_slices(int64_t M, int64_t N, int64_t K, bool int4, int group_size, int 
   int64_t mb = 1;
   while (mb < M) mb *= 2;
   return gemv_plan(mb, N, K, int4, gemv_uses_mma(mb, K, group_size > 0, mode), true, num_sms).ks;
+}
+
+void gemv_launch_info(int64_t M, int64_t N, int64_t K, bool int4, int group_size, bool split_allowed,
+                      int num_sms, int32_t* info) {
+  int64_t mb = 1;
+  while (mb < M) mb *= 2;
+  const bool mma = gemv_uses_mma(mb, K, group_size > 0, kEpiY);
+  const GemvSplit sp = gemv_plan(mb, N, K, int4, mma, split_allowed, num_sms);
+  const GemvSizes z = gemv_sizes(mb, sp, mma);
+  info[0] = static_cast<int32_t>(mb);
+  info[1] = mma ? 1 : 0;
+  info[2] = sp.ks;
+  info[3] = sp.tps;
+  info[4] = sp.Ka;
+  info[5] = static_cast<int32_t>(z.pitch);
+  info[6] = z.NS;
+  info[7] = static_cast<int32_t>(z.smem);
+  info[8] = kSmemBudget - (mma ? kRedBytes : 0) + 1024;   // the launch's dynamic shared memory cap
+  info[9] = int4 ? 2 * kBoxBytes : kBoxBytes;              // codes per weight tile row
 }
 
 size_t gemv_part_bytes(int64_t M, int64_t N, int64_t K, bool int4, int group_size, int mode,
