@@ -69,7 +69,11 @@
 // pieces of a tile run at the same time on co-resident pairs: such a launch
 // is cooperative (all pairs resident at once, or the launch fails) and never
 // exceeds the pairs the GPU holds at once.  The flags are zeroed by the
-// activation-quantization kernel that precedes every launch.
+// activation-quantization kernel that precedes every launch.  The exchange
+// pairs CTAs of equal rank, so a CTA whose 128 token rows all lie past M
+// (the second CTA of every pair at M <= 128) skips it, as do its peers.
+// The launch is a programmatic dependent of that quantization kernel: it
+// sets up barriers and tensor memory, then waits for the kernel's results.
 //
 // Exactness per tile: every partial sum of token m is bounded by
 // qmax_w * sum_k |q_a[m,k]| (qmax_w = 127 INT8, 8 INT4).  When that bound is
